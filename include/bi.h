@@ -1,0 +1,166 @@
+/*
+ * bi.h -- C ABI of the batch-invariant bf16 contraction library (GB300, sm_103a).
+ *
+ * Every output element's reduction over K runs in one fixed order: K blocks
+ * of 64 in ascending order, each block as four 16-wide tensor-core steps, an
+ * fp32 accumulator that starts from zero, then one epilogue.  The tile shape,
+ * the K order and the epilogue never depend on M, on the batch count, on the
+ * number of SMs or on which SM computes a tile; there is no split-K and no
+ * atomic accumulation.  Consequently:
+ *
+ *   INVARIANCE CONTRACT.  For fixed operation, dtypes, K, N (and, for bmm /
+ *   conv, the per-element shapes) and fixed operand layouts, output row m of
+ *   mm/addmm depends only on row m of A (and on B, bias): its bits are the
+ *   same for every M >= 1 and on every run.  The same holds per batch element
+ *   for bmm, per sample for conv2d_patch and per row for softmax_lastdim.
+ *
+ * Sources of the operations (page title, section):
+ *   mm, addmm  "Unmasking the True Culprit: Why Temperature=0 Doesn't Mean
+ *              Deterministic LLM Inference", sections "The Data-Parallel
+ *              Strategy" and "Implementation Analysis: The matmul_persistent
+ *              Function" (fixed tiles per dtype, one CTA owns the whole K
+ *              reduction of a tile, K tiles in fixed order, optional bias);
+ *              "Batch-Invariant VLAs", section "Thinky's Ops were not enough"
+ *              (aten::mm / aten::addmm replacements).
+ *   bmm        "Batch-Invariant Kernel Design: Conv2d and Attention BMM",
+ *              section "Kernel 2: Attention BMM" (rank-3 [B*H, T, D]
+ *              operands, each batch element its own base pointers and the
+ *              same ordered reduction over K).
+ *   conv2d_patch  same page, section "Kernel 1: Conv2d", and "Batch-Invariant
+ *              VLAs", section "Replacing nn.Conv2d" (per-sample unfold times
+ *              the flattened filter, plus bias).
+ *   softmax_lastdim  "ai-infra handbook: deterministic inference", section on
+ *              making normalisation and softmax batch-independent (each row
+ *              reduced by one block in a fixed order).
+ *
+ * General conventions (all entry points):
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device.
+ *     The caller allocates and owns every buffer, outputs included; the
+ *     library allocates no device memory.
+ *   - Calls are asynchronous: they validate, enqueue kernels on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream) and return.
+ *   - Argument, shape, dtype and layout errors are returned BEFORE any
+ *     launch; outputs are then untouched.  bi_last_error_message() gives
+ *     a one-line reason (thread-local).
+ *   - Strides are in ELEMENTS.  Operands are read through TMA, so a matrix
+ *     operand needs a unit stride on one of its two matrix dimensions, a
+ *     16-byte-aligned base and 16-byte-multiple other strides; anything else
+ *     returns BI_ERR_UNSUPPORTED_LAYOUT (there is no fallback path).
+ *   - Device-side failures (a bounded wait that ran out) do not hang or trap:
+ *     the kernel records a code and exits; bi_device_status() reports it.
+ */
+#ifndef BI_H_
+#define BI_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* bi_stream;
+
+typedef enum { BI_BF16 = 0, BI_F16 = 1, BI_F32 = 2 } bi_dtype;
+
+typedef enum {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,        /* null pointer, bad rank, negative size ... */
+  BI_ERR_SHAPE_MISMATCH = 2,     /* operand extents do not agree */
+  BI_ERR_UNSUPPORTED_DTYPE = 3,  /* a dtype this operation does not take */
+  BI_ERR_UNSUPPORTED_LAYOUT = 4, /* strides / alignment TMA cannot read */
+  BI_ERR_CUDA = 5,               /* a CUDA runtime or driver call failed */
+  BI_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out */
+  BI_ERR_NO_DEVICE = 7           /* no usable sm_100-family device */
+} bi_status;
+
+/* A strided view of device memory.  shape/stride entries past ndim are ignored. */
+typedef struct {
+  void* ptr;          /* device address of element [0,...,0]; NULL = absent */
+  int32_t ndim;       /* 1..4 */
+  int32_t dtype;      /* a bi_dtype value */
+  int64_t shape[4];
+  int64_t stride[4];  /* in elements */
+} bi_tensor;
+
+/*
+ * c[m,n] = sum_k a[m,k] * b[k,n]
+ *   a: [M,K] bf16, unit stride on K (row-major activations).
+ *   b: [K,N] bf16, unit stride on N (row-major weight) or on K (a transposed
+ *      view of an [N,K] weight, as torch.nn.functional.linear stores it).
+ *   c: [M,N] fp32 or bf16, unit stride on N; written, never read.
+ *   M, N, K >= 1.  The fp32 accumulator is rounded once to c's dtype (RNE).
+ */
+bi_status bi_mm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c, bi_stream stream);
+
+/*
+ * c[m,n] = (sum_k a[m,k] * b[k,n]) + bias[n]   (alpha = beta = 1)
+ *   bias: [N] bf16 or fp32, any stride; added to the fp32 accumulator after
+ *   the full K reduction, then one rounding to c's dtype.  Layouts as bi_mm.
+ */
+bi_status bi_addmm(const bi_tensor* bias, const bi_tensor* a, const bi_tensor* b,
+                   const bi_tensor* c, bi_stream stream);
+
+/*
+ * c[l,m,n] = alpha * sum_k a[l,m,k] * b[l,k,n]   for l in [0, L)
+ *   a: [L,M,K] bf16, unit stride on K;  b: [L,K,N] bf16, unit stride on N or
+ *   on K (so Q @ K^T passes K^T as a stride view);  c: [L,M,N] fp32 or bf16,
+ *   unit stride on N.  The fp32 accumulator is multiplied by alpha (fp32),
+ *   then rounded once.  Each l is an independent product.
+ */
+bi_status bi_bmm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c, float alpha,
+                 bi_stream stream);
+
+/*
+ * y = conv2d(x, w, bias), non-transposed, cross-correlation (as nn.Conv2d):
+ *   y[b,co,oh,ow] = bias[co] + sum_{ci,kh,kw} x[b, g*Cig+ci, oh*sh-ph+kh*dh, ow*sw-pw+kw*dw]
+ *                                             * w[co, ci, kh, kw]
+ *   with g = co / (Co/groups), out-of-image positions reading zero, and the
+ *   reduction index k = (ci*KH + kh)*KW + kw (the unfold order) ascending.
+ *   x: [B,C,H,W] bf16 contiguous;  w: [Co,C/groups,KH,KW] bf16 contiguous;
+ *   bias: [Co] bf16 or fp32, or NULL / ptr == NULL for none;
+ *   y: [B,Co,Ho,Wo] bf16 or fp32 contiguous, Ho = (H+2ph-dh(KH-1)-1)/sh+1.
+ *   stride, padding, dilation: {h, w}.  Each sample is computed as its own
+ *   implicit-im2col product (the patch gather happens in shared memory).
+ */
+bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tensor* bias,
+                          const bi_tensor* y, const int32_t stride[2], const int32_t padding[2],
+                          const int32_t dilation[2], int32_t groups, bi_stream stream);
+
+/*
+ * p[r,:] = softmax(s[r,:]) over the last dimension, per row r:
+ *   mx = max_j s[r,j];  e_j = expf(s[r,j] - mx);  p[r,j] = e_j / sum_j e_j,
+ *   sums in fp32 in a fixed order set by the element index only.
+ *   s: [R,N] fp32, unit stride on N;  p: [R,N] bf16 or fp32, unit stride on N.
+ */
+bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word
+ * of the current device: BI_OK, or BI_ERR_TIMEOUT when a kernel's bounded
+ * wait ran out since the last call (detail in bi_last_error_message()).
+ */
+bi_status bi_device_status(bi_stream stream);
+
+/*
+ * Test hook for the failure path: launches one block that waits, with a
+ * limit of `limit_ns` nanoseconds (1 ms .. 2 s), on a barrier that nothing
+ * ever signals.  The wait runs out, the kernel records BI_ERR_TIMEOUT and
+ * exits normally; the next bi_device_status() returns it.
+ */
+bi_status bi_debug_expire_wait(uint64_t limit_ns, bi_stream stream);
+
+/* Static, human-readable name of a status code. */
+const char* bi_status_string(bi_status status);
+
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char* bi_last_error_message(void);
+
+/* ABI version of this header (incremented on any signature change). */
+int32_t bi_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_H_ */

@@ -1,9 +1,15 @@
 """Batch-invariant bf16 contractions for GB300 (sm_103a).
 
-The operations (``mm``, ``addmm``, ``bmm``, ``conv2d_patch``,
-``softmax_lastdim``) run in hand-written CUDA kernels behind the C ABI
-declared in ``include/bi.h``; this package only marshals torch tensors into
-that ABI.  The shared library is loaded on first use and an operation raises
-if it is missing -- there is no CPU or library fallback.
+The operations run in hand-written CUDA kernels behind the C ABI declared in
+``include/bi.h``; ``binding`` only marshals torch tensors into that ABI, with
+the same names as the C entry points:
+
+    bi_mm, bi_addmm, bi_bmm, bi_conv2d_patch, bi_softmax_lastdim,
+    bi_device_status
+
+The shared library is loaded on first use; a call raises if it is missing --
+there is no CPU or library fallback.
 """
 from . import inputs  # noqa: F401  (seeded input generators; no arithmetic)
+from .binding import (BiError, bi_addmm, bi_bmm, bi_conv2d_patch, bi_device_status,  # noqa: F401
+                      bi_mm, bi_softmax_lastdim)

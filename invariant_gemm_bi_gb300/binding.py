@@ -1,0 +1,214 @@
+"""ctypes binding of the C ABI in ``include/bi.h`` (argument marshalling only).
+
+Each function takes CUDA torch tensors, describes them as ``bi_tensor``
+structs (pointer, shape, element strides, dtype code), allocates the output
+with torch when ``out`` is not given, and calls the entry point of the same
+name on the current torch stream.  All arithmetic happens in the library's
+CUDA kernels; a missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+BI_OK = 0
+BI_ERR_INVALID_ARG = 1
+BI_ERR_SHAPE_MISMATCH = 2
+BI_ERR_UNSUPPORTED_DTYPE = 3
+BI_ERR_UNSUPPORTED_LAYOUT = 4
+BI_ERR_CUDA = 5
+BI_ERR_TIMEOUT = 6
+BI_ERR_NO_DEVICE = 7
+
+EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
+            "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
+            "bi_last_error_message", "bi_abi_version")
+
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+
+
+class BiTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("ndim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class BiError(RuntimeError):
+    def __init__(self, op: str, status: int, name: str, detail: str):
+        super().__init__(f"{op}: {name}: {detail}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Loads the shared library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"CUDA library {p} is missing: run invariant_gemm_bi_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            ptr = ctypes.POINTER(BiTensor)
+            i32x2 = ctypes.POINTER(ctypes.c_int32)
+            st = ctypes.c_int
+            sig = {
+                "bi_mm": ([ptr, ptr, ptr, ctypes.c_void_p], st),
+                "bi_addmm": ([ptr, ptr, ptr, ptr, ctypes.c_void_p], st),
+                "bi_bmm": ([ptr, ptr, ptr, ctypes.c_float, ctypes.c_void_p], st),
+                "bi_conv2d_patch": ([ptr, ptr, ptr, ptr, i32x2, i32x2, i32x2, ctypes.c_int32,
+                                     ctypes.c_void_p], st),
+                "bi_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
+                "bi_device_status": ([ctypes.c_void_p], st),
+                "bi_debug_expire_wait": ([ctypes.c_uint64, ctypes.c_void_p], st),
+                "bi_status_string": ([st], ctypes.c_char_p),
+                "bi_last_error_message": ([], ctypes.c_char_p),
+                "bi_abi_version": ([], ctypes.c_int32),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _desc(t: torch.Tensor | None, name: str) -> BiTensor | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: expected a CUDA tensor, got {t.device}")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"{name}: unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError(f"{name}: rank {t.dim()} > 4")
+    d = BiTensor()
+    d.ptr = t.data_ptr() if t.numel() else (t.data_ptr() or None)
+    d.ndim = t.dim()
+    d.dtype = _DTYPES[t.dtype]
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d: BiTensor | None):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(lib, op: str, status: int):
+    if status != BI_OK:
+        name = lib.bi_status_string(status).decode()
+        detail = lib.bi_last_error_message().decode()
+        raise BiError(op, status, name, detail)
+
+
+def bi_mm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+          out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """out[m,n] = sum_k a[m,k] b[k,n]  (bf16 inputs, fp32 accumulation)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype, device=a.device)
+    da, db, dc = _desc(a, "a"), _desc(b, "b"), _desc(out, "out")
+    _check(lib, "bi_mm", lib.bi_mm(_ref(da), _ref(db), _ref(dc), _stream(stream)))
+    return out
+
+
+def bi_addmm(bias: torch.Tensor, a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+             out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """out[m,n] = sum_k a[m,k] b[k,n] + bias[n]."""
+    lib = load()
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype, device=a.device)
+    dbias, da, db, dc = _desc(bias, "bias"), _desc(a, "a"), _desc(b, "b"), _desc(out, "out")
+    _check(lib, "bi_addmm", lib.bi_addmm(_ref(dbias), _ref(da), _ref(db), _ref(dc), _stream(stream)))
+    return out
+
+
+def bi_bmm(a: torch.Tensor, b: torch.Tensor, alpha: float = 1.0, out: torch.Tensor | None = None,
+           out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """out[l] = alpha * a[l] @ b[l]."""
+    lib = load()
+    if out is None:
+        out = torch.empty((a.shape[0], a.shape[1], b.shape[2]), dtype=out_dtype, device=a.device)
+    da, db, dc = _desc(a, "a"), _desc(b, "b"), _desc(out, "out")
+    _check(lib, "bi_bmm", lib.bi_bmm(_ref(da), _ref(db), _ref(dc), float(alpha), _stream(stream)))
+    return out
+
+
+def _pair(v):
+    return (int(v), int(v)) if isinstance(v, int) else (int(v[0]), int(v[1]))
+
+
+def conv_out_hw(h, w, kh, kw, stride, padding, dilation):
+    sh, sw = _pair(stride)
+    ph, pw = _pair(padding)
+    dh, dw = _pair(dilation)
+    return (h + 2 * ph - dh * (kh - 1) - 1) // sh + 1, (w + 2 * pw - dw * (kw - 1) - 1) // sw + 1
+
+
+def bi_conv2d_patch(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None, stride=1,
+                    padding=0, dilation=1, groups: int = 1, out: torch.Tensor | None = None,
+                    out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """2-D convolution (as nn.Conv2d) computed per sample as an implicit-im2col product."""
+    lib = load()
+    if out is None:
+        ho, wo = conv_out_hw(x.shape[2], x.shape[3], w.shape[2], w.shape[3], stride, padding, dilation)
+        out = torch.empty((x.shape[0], w.shape[0], max(ho, 0), max(wo, 0)), dtype=out_dtype,
+                          device=x.device)
+    arr = ctypes.c_int32 * 2
+    st, pd, dl = arr(*_pair(stride)), arr(*_pair(padding)), arr(*_pair(dilation))
+    dx, dw_, db, dy = _desc(x, "x"), _desc(w, "w"), _desc(bias, "bias"), _desc(out, "out")
+    _check(lib, "bi_conv2d_patch",
+           lib.bi_conv2d_patch(_ref(dx), _ref(dw_), _ref(db), _ref(dy), st, pd, dl, int(groups),
+                               _stream(stream)))
+    return out
+
+
+def bi_softmax_lastdim(s: torch.Tensor, out: torch.Tensor | None = None,
+                       out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """Row softmax of a 2-D fp32 tensor over its last dimension."""
+    lib = load()
+    if out is None:
+        out = torch.empty(s.shape, dtype=out_dtype, device=s.device)
+    ds, dp = _desc(s, "s"), _desc(out, "out")
+    _check(lib, "bi_softmax_lastdim", lib.bi_softmax_lastdim(_ref(ds), _ref(dp), _stream(stream)))
+    return out
+
+
+def bi_device_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status word as a status code."""
+    lib = load()
+    return int(lib.bi_device_status(_stream(stream)))
+
+
+def bi_debug_expire_wait(limit_ns: int, stream=None) -> None:
+    """Launches the bounded-wait test kernel (a wait that nothing ends)."""
+    lib = load()
+    _check(lib, "bi_debug_expire_wait", lib.bi_debug_expire_wait(int(limit_ns), _stream(stream)))
+
+
+def last_error_message() -> str:
+    return load().bi_last_error_message().decode()
+
+
+def status_string(status: int) -> str:
+    return load().bi_status_string(int(status)).decode()

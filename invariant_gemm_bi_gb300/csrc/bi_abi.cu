@@ -1,0 +1,512 @@
+// bi_abi.cu -- the C ABI declared in include/bi.h: argument validation (all of
+// it before any launch), operand-layout normalisation, per-device state (SM
+// count, the device status word), TMA descriptor encoding and error reporting.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/bi.h"
+#include "bi_common.h"
+#include "bi_launch.h"
+
+// First device-side failure since the last bi_device_status() (0 = none).
+__device__ unsigned int g_bi_status_word;
+
+namespace bi {
+
+namespace {
+
+thread_local std::string t_last_error;
+std::mutex g_mu;
+
+constexpr int kMaxDevices = 64;
+struct DevState {
+  bool ready = false;
+  bi_status status = BI_OK;
+  std::string why;
+  int num_sms = 0;
+  unsigned int* status_word = nullptr;
+  bool smem_set[8] = {};
+};
+DevState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+bi_status finish(bi_status st, const std::string& why) {
+  t_last_error = (st == BI_OK) ? std::string() : why;
+  return st;
+}
+
+}  // namespace
+
+bi_status current_device_info(DeviceInfo* info, std::string* why) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0) {
+    *why = std::string("no CUDA device: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    return BI_ERR_NO_DEVICE;
+  }
+  if (dev >= kMaxDevices) {
+    *why = "device ordinal out of range";
+    return BI_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) {
+      d.status = BI_ERR_NO_DEVICE;
+      d.why = "device " + std::to_string(dev) + " has compute capability " + std::to_string(major) +
+              "." + std::to_string(minor) + "; this library is built for sm_103a only";
+    } else {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_bi_status_word);
+      if (e != cudaSuccess) {
+        d.status = BI_ERR_CUDA;
+        d.why = std::string("status word: ") + cudaGetErrorString(e);
+      } else {
+        d.status = BI_OK;
+        d.num_sms = sms;
+        d.status_word = reinterpret_cast<unsigned int*>(addr);
+      }
+    }
+    d.ready = true;
+  }
+  if (d.status != BI_OK) {
+    *why = d.why;
+    return d.status;
+  }
+  info->device = dev;
+  info->num_sms = d.num_sms;
+  info->status_word = d.status_word;
+  return BI_OK;
+}
+
+bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                       const cuuint32_t* elem_strides, std::string* why) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+      g_encode_tried = true;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      cudaGetLastError();
+    }
+  }
+  if (!g_encode) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, ptr, dims, strides_bytes, box,
+                        elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+cudaError_t set_smem_once(const void* func, int bytes, int slot) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (d.smem_set[slot]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) d.smem_set[slot] = true;
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// Validation helpers
+// ---------------------------------------------------------------------------
+namespace {
+
+int elem_size(int dtype) { return dtype == BI_F32 ? 4 : 2; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bi_status check_tensor(const bi_tensor* t, const char* name, int ndim, std::string* why) {
+  if (!t) {
+    *why = std::string(name) + ": null tensor descriptor";
+    return BI_ERR_INVALID_ARG;
+  }
+  if (t->ndim != ndim) {
+    *why = std::string(name) + ": expected rank " + std::to_string(ndim) + ", got " +
+           std::to_string(t->ndim);
+    return BI_ERR_INVALID_ARG;
+  }
+  if (t->dtype != BI_BF16 && t->dtype != BI_F16 && t->dtype != BI_F32) {
+    *why = std::string(name) + ": unknown dtype code " + std::to_string(t->dtype);
+    return BI_ERR_UNSUPPORTED_DTYPE;
+  }
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0 || t->shape[i] > INT32_MAX) {
+      *why = std::string(name) + ": dimension " + std::to_string(i) + " out of range";
+      return BI_ERR_INVALID_ARG;
+    }
+    if (t->stride[i] < 0) {
+      *why = std::string(name) + ": negative strides are not supported";
+      return BI_ERR_UNSUPPORTED_LAYOUT;
+    }
+  }
+  return BI_OK;
+}
+
+int64_t numel(const bi_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+bi_status need_ptr(const bi_tensor* t, const char* name, std::string* why) {
+  if (!t->ptr) {
+    *why = std::string(name) + ": null data pointer";
+    return BI_ERR_INVALID_ARG;
+  }
+  return BI_OK;
+}
+
+bool is_contiguous(const bi_tensor* t) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->stride[i] != expect) return false;
+    expect *= t->shape[i];
+  }
+  return true;
+}
+
+// Shared by mm / addmm (batched = false) and bmm (batched = true).
+bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor* b,
+                      const bi_tensor* c, float alpha, bool batched, cudaStream_t stream,
+                      std::string* why) {
+  const int nd = batched ? 3 : 2;
+  bi_status st;
+  if ((st = check_tensor(a, "a", nd, why)) != BI_OK) return st;
+  if ((st = check_tensor(b, "b", nd, why)) != BI_OK) return st;
+  if ((st = check_tensor(c, "c", nd, why)) != BI_OK) return st;
+  if (a->dtype != BI_BF16 || b->dtype != BI_BF16) {
+    *why = "a and b must both be bf16";
+    return BI_ERR_UNSUPPORTED_DTYPE;
+  }
+  if (c->dtype != BI_BF16 && c->dtype != BI_F32) {
+    *why = "c must be bf16 or fp32";
+    return BI_ERR_UNSUPPORTED_DTYPE;
+  }
+  const int o = batched ? 1 : 0;  // offset of the matrix dims
+  const int64_t L = batched ? a->shape[0] : 1;
+  const int64_t M = a->shape[o], K = a->shape[o + 1];
+  const int64_t N = b->shape[o + 1];
+  if (b->shape[o] != K) {
+    *why = "inner dimensions differ: a has K=" + std::to_string(K) + ", b has K=" +
+           std::to_string(b->shape[o]);
+    return BI_ERR_SHAPE_MISMATCH;
+  }
+  if (c->shape[o] != M || c->shape[o + 1] != N ||
+      (batched && (b->shape[0] != L || c->shape[0] != L))) {
+    *why = "output / batch extents do not match the operands";
+    return BI_ERR_SHAPE_MISMATCH;
+  }
+  int bias_kind = 0;
+  int64_t bias_stride = 0;
+  if (bias && bias->ptr) {
+    if ((st = check_tensor(bias, "bias", 1, why)) != BI_OK) return st;
+    if (bias->shape[0] != N) {
+      *why = "bias must have N elements";
+      return BI_ERR_SHAPE_MISMATCH;
+    }
+    if (bias->dtype == BI_BF16)
+      bias_kind = 1;
+    else if (bias->dtype == BI_F32)
+      bias_kind = 2;
+    else {
+      *why = "bias must be bf16 or fp32";
+      return BI_ERR_UNSUPPORTED_DTYPE;
+    }
+    bias_stride = bias->stride[0];
+    if (!aligned(bias->ptr, elem_size(bias->dtype))) {
+      *why = "bias pointer is not aligned to its element size";
+      return BI_ERR_UNSUPPORTED_LAYOUT;
+    }
+  }
+  if (L == 0 || M == 0 || N == 0) return BI_OK;  // nothing to compute
+  if ((st = need_ptr(c, "c", why)) != BI_OK) return st;
+
+  GemmProblem g;
+  memset(&g, 0, sizeof(g));
+  g.L = L;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.alpha = alpha;
+  g.bias = bias_kind ? bias->ptr : nullptr;
+  g.bias_kind = bias_kind;
+  g.bias_stride = bias_stride;
+  g.c = c->ptr;
+  g.out_f32 = c->dtype == BI_F32;
+  const int cesz = elem_size(c->dtype);
+  if (!(N == 1 || c->stride[o + 1] == 1)) {
+    *why = "c needs a unit stride on N";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  g.ldc = (M == 1) ? N : c->stride[o];
+  g.c_batch = batched ? c->stride[0] : 0;
+  if (!aligned(c->ptr, cesz)) {
+    *why = "c pointer is not aligned to its element size";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  g.vec_store = aligned(c->ptr, 16) && (g.ldc * cesz) % 16 == 0 &&
+                (L <= 1 || (g.c_batch * cesz) % 16 == 0);
+
+  if (K == 0) return launch_fill_bias(g, stream, why);
+
+  if ((st = need_ptr(a, "a", why)) != BI_OK) return st;
+  if ((st = need_ptr(b, "b", why)) != BI_OK) return st;
+
+  // A: unit stride on K; row stride a 16-byte multiple; 16-byte aligned base.
+  if (!(K == 1 || a->stride[o + 1] == 1)) {
+    *why = "a needs a unit stride on K (row-major activations)";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  g.a = a->ptr;
+  g.lda = (M == 1) ? (int64_t)round_up_u64((uint64_t)K, 8) : a->stride[o];
+  g.a_batch = batched ? a->stride[0] : 0;
+  if (!aligned(a->ptr, 16) || (g.lda * 2) % 16 != 0 || g.lda == 0 ||
+      (L > 1 && ((g.a_batch * 2) % 16 != 0 || g.a_batch == 0))) {
+    *why = "a: base must be 16-byte aligned and its row / batch strides multiples of 8 elements";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  // B: unit stride on N (MN-major) or on K (K-major, a transposed view).
+  const bool mn_ok = (N == 1) || b->stride[o + 1] == 1;
+  const bool k_ok = (K == 1) || b->stride[o] == 1;
+  g.b = b->ptr;
+  g.b_batch = batched ? b->stride[0] : 0;
+  if (mn_ok && (N > 1 || !k_ok)) {
+    g.b_mn_major = 1;
+    g.ldb = (K == 1) ? (int64_t)round_up_u64((uint64_t)N, 8) : b->stride[o];
+  } else if (k_ok) {
+    g.b_mn_major = 0;
+    g.ldb = (N == 1) ? (int64_t)round_up_u64((uint64_t)K, 8) : b->stride[o + 1];
+  } else {
+    *why = "b needs a unit stride on N or on K";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  if (!aligned(b->ptr, 16) || (g.ldb * 2) % 16 != 0 || g.ldb == 0 ||
+      (L > 1 && ((g.b_batch * 2) % 16 != 0 || g.b_batch == 0))) {
+    *why = "b: base must be 16-byte aligned and its non-unit strides multiples of 8 elements";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  (void)numel;
+  return launch_gemm(g, stream, why);
+}
+
+}  // namespace
+}  // namespace bi
+
+// ---------------------------------------------------------------------------
+// C entry points
+// ---------------------------------------------------------------------------
+using namespace bi;
+
+extern "C" bi_status bi_mm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c,
+                           bi_stream stream) {
+  std::string why;
+  bi_status st = matmul_impl(nullptr, a, b, c, 1.0f, false, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_addmm(const bi_tensor* bias, const bi_tensor* a, const bi_tensor* b,
+                              const bi_tensor* c, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if (!bias || !bias->ptr) {
+    why = "bias: null (use bi_mm for a product without bias)";
+    st = BI_ERR_INVALID_ARG;
+  } else {
+    st = matmul_impl(bias, a, b, c, 1.0f, false, (cudaStream_t)stream, &why);
+  }
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_bmm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c,
+                            float alpha, bi_stream stream) {
+  std::string why;
+  bi_status st = matmul_impl(nullptr, a, b, c, alpha, true, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tensor* bias,
+                                     const bi_tensor* y, const int32_t stride[2],
+                                     const int32_t padding[2], const int32_t dilation[2],
+                                     int32_t groups, bi_stream stream) {
+  std::string why;
+  bi_status st = BI_OK;
+  auto fail = [&](bi_status s, const std::string& m) {
+    why = m;
+    return finish(s, why);
+  };
+  if ((st = check_tensor(x, "x", 4, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(w, "w", 4, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(y, "y", 4, &why)) != BI_OK) return finish(st, why);
+  if (!stride || !padding || !dilation) return fail(BI_ERR_INVALID_ARG, "stride/padding/dilation: null");
+  if (x->dtype != BI_BF16 || w->dtype != BI_BF16)
+    return fail(BI_ERR_UNSUPPORTED_DTYPE, "x and w must be bf16");
+  if (y->dtype != BI_BF16 && y->dtype != BI_F32)
+    return fail(BI_ERR_UNSUPPORTED_DTYPE, "y must be bf16 or fp32");
+  if (groups < 1) return fail(BI_ERR_INVALID_ARG, "groups must be >= 1");
+  if (stride[0] < 1 || stride[1] < 1 || dilation[0] < 1 || dilation[1] < 1 || padding[0] < 0 ||
+      padding[1] < 0)
+    return fail(BI_ERR_INVALID_ARG, "stride and dilation must be >= 1, padding >= 0");
+  const int64_t B = x->shape[0], C = x->shape[1], H = x->shape[2], W = x->shape[3];
+  const int64_t Co = w->shape[0], Cig = w->shape[1], KH = w->shape[2], KW = w->shape[3];
+  if (C % groups != 0 || Co % groups != 0 || Cig * groups != C)
+    return fail(BI_ERR_SHAPE_MISMATCH, "channels do not divide into groups as w expects");
+  if (KH < 1 || KW < 1) return fail(BI_ERR_INVALID_ARG, "kernel extents must be >= 1");
+  const int64_t Ho = (H + 2 * padding[0] - (int64_t)dilation[0] * (KH - 1) - 1) / stride[0] + 1;
+  const int64_t Wo = (W + 2 * padding[1] - (int64_t)dilation[1] * (KW - 1) - 1) / stride[1] + 1;
+  if (H + 2 * padding[0] - (int64_t)dilation[0] * (KH - 1) - 1 < 0 ||
+      W + 2 * padding[1] - (int64_t)dilation[1] * (KW - 1) - 1 < 0)
+    return fail(BI_ERR_SHAPE_MISMATCH, "kernel window larger than the padded image");
+  if (y->shape[0] != B || y->shape[1] != Co || y->shape[2] != Ho || y->shape[3] != Wo)
+    return fail(BI_ERR_SHAPE_MISMATCH, "y must be [B, Co, Ho, Wo] = [" + std::to_string(B) + ", " +
+                                           std::to_string(Co) + ", " + std::to_string(Ho) + ", " +
+                                           std::to_string(Wo) + "]");
+  if (!is_contiguous(x) || !is_contiguous(w) || !is_contiguous(y))
+    return fail(BI_ERR_UNSUPPORTED_LAYOUT, "x, w and y must be contiguous (NCHW)");
+  if (Ho * Wo > INT32_MAX || Cig * KH * KW > INT32_MAX)
+    return fail(BI_ERR_INVALID_ARG, "per-sample problem too large");
+  int bias_kind = 0;
+  if (bias && bias->ptr) {
+    if ((st = check_tensor(bias, "bias", 1, &why)) != BI_OK) return finish(st, why);
+    if (bias->shape[0] != Co) return fail(BI_ERR_SHAPE_MISMATCH, "bias must have Co elements");
+    if (bias->stride[0] != 1 && Co > 1) return fail(BI_ERR_UNSUPPORTED_LAYOUT, "bias must be contiguous");
+    if (bias->dtype == BI_BF16)
+      bias_kind = 1;
+    else if (bias->dtype == BI_F32)
+      bias_kind = 2;
+    else
+      return fail(BI_ERR_UNSUPPORTED_DTYPE, "bias must be bf16 or fp32");
+  }
+  if (B == 0 || Co == 0) return finish(BI_OK, why);
+  if (!x->ptr || !w->ptr || !y->ptr) return fail(BI_ERR_INVALID_ARG, "null data pointer");
+  if (!aligned(x->ptr, 2) || !aligned(w->ptr, 2) || !aligned(y->ptr, y->dtype == BI_F32 ? 4 : 2))
+    return fail(BI_ERR_UNSUPPORTED_LAYOUT, "pointers must be aligned to their element size");
+  if (C == 0 || KH * KW == 0) return fail(BI_ERR_INVALID_ARG, "empty reduction (C == 0)");
+  ConvProblem cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.x = x->ptr;
+  cp.w = w->ptr;
+  cp.bias = bias_kind ? bias->ptr : nullptr;
+  cp.bias_kind = bias_kind;
+  cp.y = y->ptr;
+  cp.out_f32 = y->dtype == BI_F32;
+  cp.B = B;
+  cp.C = C;
+  cp.H = H;
+  cp.W = W;
+  cp.Co = Co;
+  cp.KH = KH;
+  cp.KW = KW;
+  cp.Ho = Ho;
+  cp.Wo = Wo;
+  cp.sh = stride[0];
+  cp.sw = stride[1];
+  cp.ph = padding[0];
+  cp.pw = padding[1];
+  cp.dh = dilation[0];
+  cp.dw = dilation[1];
+  cp.groups = groups;
+  st = launch_conv(cp, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if ((st = check_tensor(s, "s", 2, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(p, "p", 2, &why)) != BI_OK) return finish(st, why);
+  if (s->dtype != BI_F32) return finish(BI_ERR_UNSUPPORTED_DTYPE, "s must be fp32");
+  if (p->dtype != BI_BF16 && p->dtype != BI_F32)
+    return finish(BI_ERR_UNSUPPORTED_DTYPE, "p must be bf16 or fp32");
+  if (s->shape[0] != p->shape[0] || s->shape[1] != p->shape[1])
+    return finish(BI_ERR_SHAPE_MISMATCH, "s and p must have the same shape");
+  const int64_t R = s->shape[0], N = s->shape[1];
+  if (R == 0 || N == 0) return finish(BI_OK, why);
+  if (!s->ptr || !p->ptr) return finish(BI_ERR_INVALID_ARG, "null data pointer");
+  if ((N > 1 && (s->stride[1] != 1 || p->stride[1] != 1)))
+    return finish(BI_ERR_UNSUPPORTED_LAYOUT, "s and p need a unit stride on the last dimension");
+  if (!aligned(s->ptr, 4) || !aligned(p->ptr, p->dtype == BI_F32 ? 4 : 2))
+    return finish(BI_ERR_UNSUPPORTED_LAYOUT, "pointers must be aligned to their element size");
+  SoftmaxParams sp;
+  sp.s = reinterpret_cast<const float*>(s->ptr);
+  sp.p = p->ptr;
+  sp.R = R;
+  sp.N = N;
+  sp.ld_s = (R == 1) ? N : s->stride[0];
+  sp.ld_p = (R == 1) ? N : p->stride[0];
+  sp.out_f32 = p->dtype == BI_F32;
+  st = launch_softmax(sp, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_device_status(bi_stream stream) {
+  std::string why;
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, &why);
+  if (st != BI_OK) return finish(st, why);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return finish(BI_ERR_CUDA, std::string("stream sync: ") + cudaGetErrorString(e));
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, dev.status_word, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return finish(BI_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));
+  if (v == 0) return finish(BI_OK, why);
+  e = cudaMemset(dev.status_word, 0, sizeof(v));
+  if (e != cudaSuccess) return finish(BI_ERR_CUDA, std::string("status clear: ") + cudaGetErrorString(e));
+  static const char* kSites[] = {"?", "producer waiting for a free stage", "MMA waiting for a full stage",
+                                 "MMA waiting for a free accumulator", "epilogue waiting for an accumulator",
+                                 "draining in-flight work", "debug wait", "conv producer waiting for a free stage"};
+  const unsigned site = (v >> 8) & 0xFF;
+  why = std::string("device wait ran out: ") + (site < 8 ? kSites[site] : "?");
+  return finish((bi_status)(v & 0xFF), why);
+}
+
+extern "C" bi_status bi_debug_expire_wait(uint64_t limit_ns, bi_stream stream) {
+  std::string why;
+  if (limit_ns < 1000000ull || limit_ns > 2000000000ull)
+    return finish(BI_ERR_INVALID_ARG, "limit_ns must be within [1 ms, 2 s]");
+  bi_status st = launch_debug_wait(limit_ns, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" const char* bi_status_string(bi_status s) {
+  switch (s) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG";
+    case BI_ERR_SHAPE_MISMATCH: return "BI_ERR_SHAPE_MISMATCH";
+    case BI_ERR_UNSUPPORTED_DTYPE: return "BI_ERR_UNSUPPORTED_DTYPE";
+    case BI_ERR_UNSUPPORTED_LAYOUT: return "BI_ERR_UNSUPPORTED_LAYOUT";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA";
+    case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT";
+    case BI_ERR_NO_DEVICE: return "BI_ERR_NO_DEVICE";
+  }
+  return "BI_ERR_UNKNOWN";
+}
+
+extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
+
+extern "C" int32_t bi_abi_version(void) { return 1; }

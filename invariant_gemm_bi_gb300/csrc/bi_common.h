@@ -1,0 +1,80 @@
+// bi_common.h -- definitions shared by the host launchers and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace bi {
+
+// ---------------------------------------------------------------------------
+// The one fixed bf16 tile.  Never chosen from M, the batch count or the SM
+// count: every output element of every call sees the same instruction
+// sequence (128 x BN x 16 UMMA steps, K blocks of 64 in ascending order).
+// ---------------------------------------------------------------------------
+#ifndef BI_TILE_N
+#define BI_TILE_N 256
+#endif
+constexpr int kBM = 128;        // UMMA M: rows of A / output rows per tile
+constexpr int kBN = BI_TILE_N;  // UMMA N: output columns per tile
+constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kUmmaK = 16;      // K per tcgen05.mma (kind::f16)
+constexpr int kGroupM = 16;     // raster group height (L2 reuse only; no numerical effect)
+
+// Device status codes (the status word holds the first failure of a device).
+// Low byte: a bi_status value; next byte: where it happened.
+enum : unsigned int {
+  kSiteProducerEmpty = 1,
+  kSiteMmaFull = 2,
+  kSiteMmaTmemEmpty = 3,
+  kSiteEpilogueTmemFull = 4,
+  kSiteDrain = 5,
+  kSiteDebugWait = 6,
+  kSiteConvProducer = 7,
+};
+__host__ __device__ constexpr unsigned int status_code(unsigned int bi_err, unsigned int site) {
+  return bi_err | (site << 8);
+}
+
+struct GemmParams {
+  CUtensorMap tma_a;  // A as [L][M][K] bf16, box {64, 128, 1}, 128B swizzle
+  CUtensorMap tma_b;  // K-major B as [L][N][K], box {64, BN, 1}; MN-major as [L][K][N], box {64, 64, 1}
+  void* c;
+  const void* bias;
+  int64_t ldc;             // elements
+  int64_t c_batch_stride;  // elements
+  int64_t bias_stride;     // elements
+  float alpha;
+  int32_t M, N, K, L;
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles;
+  int32_t out_f32;    // 1: fp32 output, 0: bf16 output
+  int32_t bias_kind;  // 0: none, 1: bf16, 2: fp32
+  int32_t vec_store;  // 1: every output row start is 16-byte aligned
+  int32_t pad_;
+  unsigned int* status_word;
+  uint64_t wait_limit_ns;
+};
+
+struct ConvParams {
+  const uint16_t* x;   // [B][C][H][W] bf16 contiguous
+  const uint16_t* w;   // [Co][C/groups][KH][KW] bf16 contiguous
+  const void* bias;    // [Co] or null
+  void* y;             // [B][Co][Ho][Wo] contiguous
+  int32_t B, C, H, W, Co, KH, KW, Ho, Wo;
+  int32_t sh, sw, ph, pw, dh, dw, groups;
+  int32_t Cig, Cog, Kg;       // channels per group in/out, reduction length per group
+  int32_t P;                  // Ho*Wo output positions per sample
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles;  // per (sample, group) tile space
+  int32_t out_f32, bias_kind, vec_store;
+  unsigned int* status_word;
+  uint64_t wait_limit_ns;
+};
+
+struct SoftmaxParams {
+  const float* s;
+  void* p;
+  int64_t R, N;
+  int64_t ld_s, ld_p;  // elements
+  int32_t out_f32;
+};
+
+}  // namespace bi

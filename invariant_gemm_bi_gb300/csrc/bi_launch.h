@@ -1,0 +1,82 @@
+// bi_launch.h -- host-side interfaces between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "../../include/bi.h"
+#include "bi_common.h"
+
+namespace bi {
+
+// Bound on every device-side wait: far above any legitimate wait (a tile's
+// whole K loop takes well under a millisecond), short enough that a broken
+// pipeline returns an error instead of holding the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+inline uint64_t round_up_u64(uint64_t v, uint64_t m) { return (v + m - 1) / m * m; }
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  unsigned int* status_word;  // device address of this device's status word
+};
+
+// Fills `info` for the current device (cached per device).  Fails with
+// BI_ERR_NO_DEVICE unless the device is compute capability 10.3 (sm_103).
+bi_status current_device_info(DeviceInfo* info, std::string* why);
+
+// cuTensorMapEncodeTiled for a bf16 tensor with 128-byte swizzle and zero
+// fill out of bounds (driver entry point resolved once through the runtime).
+bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                       const cuuint32_t* elem_strides, std::string* why);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, slot).
+cudaError_t set_smem_once(const void* func, int bytes, int slot);
+
+// A normalised matrix-product problem: c[l] = alpha * a[l] @ b[l] (+ bias).
+struct GemmProblem {
+  const void* a;  // bf16, [L][M][K], unit stride on K
+  int64_t lda, a_batch;
+  const void* b;  // bf16; b_mn_major: b[l][k][n] at k*ldb + n; else at n*ldb + k
+  int64_t ldb, b_batch;
+  int b_mn_major;
+  void* c;  // [L][M][N], unit stride on N
+  int64_t ldc, c_batch;
+  int out_f32;
+  const void* bias;  // per column n, or null
+  int64_t bias_stride;
+  int bias_kind;  // 0 none, 1 bf16, 2 fp32
+  float alpha;
+  int64_t L, M, N, K;
+  int vec_store;
+};
+
+bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* why);
+
+struct ConvProblem {
+  const void* x;
+  const void* w;
+  const void* bias;
+  int bias_kind;
+  void* y;
+  int out_f32;
+  int64_t B, C, H, W, Co, KH, KW, Ho, Wo;
+  int sh, sw, ph, pw, dh, dw, groups;
+};
+
+bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* why);
+
+bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::string* why);
+
+bi_status launch_fill_bias(const GemmProblem& g, cudaStream_t stream, std::string* why);
+
+bi_status launch_debug_wait(uint64_t limit_ns, cudaStream_t stream, std::string* why);
+
+}  // namespace bi

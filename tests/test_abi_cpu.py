@@ -1,0 +1,150 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+it exports every entry point include/bi.h declares, and argument / shape /
+dtype / layout errors come back as status codes before anything is launched
+(the descriptors below point at fake addresses that are never touched)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from invariant_gemm_bi_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "bi.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _header_functions()
+    for n in ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
+              "bi_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+    assert set(_header_functions()) == set(binding.EXPORTED)
+
+
+def test_library_has_no_oracle_or_host_math_dependency():
+    # The product library must not link the oracle (it is test infrastructure).
+    data = open(build.LIB_PATH, "rb").read()
+    assert b"bio_mm" not in data and b"libbi_oracle" not in data
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "BI_OK"
+    assert binding.status_string(6) == "BI_ERR_TIMEOUT"
+    assert lib.bi_abi_version() == 1
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def _t(shape, stride=None, dtype=0, ptr=FAKE):
+    d = binding.BiTensor()
+    d.ptr = ptr
+    d.ndim = len(shape)
+    d.dtype = dtype
+    if stride is None:
+        stride, s = [], 1
+        for n in reversed(shape):
+            stride.insert(0, s)
+            s *= n
+    for i, (n, st) in enumerate(zip(shape, stride)):
+        d.shape[i] = n
+        d.stride[i] = st
+    return d
+
+
+def _r(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _mm(lib, a, b, c):
+    return lib.bi_mm(_r(a), _r(b), _r(c), None)
+
+
+def test_mm_validation_errors(lib):
+    ok_a, ok_b, ok_c = _t([4, 64]), _t([64, 32]), _t([4, 32], dtype=2)
+    # inner dimension mismatch
+    assert _mm(lib, ok_a, _t([48, 32]), ok_c) == binding.BI_ERR_SHAPE_MISMATCH
+    # output extent mismatch
+    assert _mm(lib, ok_a, ok_b, _t([4, 33], dtype=2)) == binding.BI_ERR_SHAPE_MISMATCH
+    # fp32 / fp16 inputs are not taken
+    assert _mm(lib, _t([4, 64], dtype=2), ok_b, ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert _mm(lib, _t([4, 64], dtype=1), _t([64, 32], dtype=1), ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # wrong rank
+    assert _mm(lib, _t([4, 64, 1]), ok_b, ok_c) == binding.BI_ERR_INVALID_ARG
+    # null descriptor
+    assert lib.bi_mm(None, _r(ok_b), _r(ok_c), None) == binding.BI_ERR_INVALID_ARG
+    # A without a unit stride on K (column-major activations)
+    assert _mm(lib, _t([4, 64], [1, 4]), ok_b, ok_c) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # A row stride not a multiple of 8 elements (16 bytes)
+    assert _mm(lib, _t([4, 60], [60, 1]), _t([60, 32]), ok_c) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # misaligned base
+    assert _mm(lib, _t([4, 64], ptr=FAKE + 2), ok_b, ok_c) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # B with neither unit stride
+    assert _mm(lib, ok_a, _t([64, 32], [64, 2]), ok_c) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # output without unit stride on N
+    assert _mm(lib, ok_a, ok_b, _t([4, 32], [1, 4], dtype=2)) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # negative stride
+    assert _mm(lib, ok_a, _t([64, 32], [-32, 1]), ok_c) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert "stride" in binding.last_error_message()
+
+
+def test_empty_problems_are_no_ops_without_touching_the_device(lib):
+    # M == 0 / N == 0: nothing to compute, OK before any CUDA call
+    assert _mm(lib, _t([0, 64]), _t([64, 32]), _t([0, 32], dtype=2)) == binding.BI_OK
+    assert _mm(lib, _t([4, 64]), _t([64, 0]), _t([4, 0], dtype=2)) == binding.BI_OK
+    assert lib.bi_softmax_lastdim(_r(_t([0, 8], dtype=2)), _r(_t([0, 8])), None) == binding.BI_OK
+
+
+def test_valid_call_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _mm(lib, _t([4, 64]), _t([64, 32]), _t([4, 32], dtype=2))
+    assert st == binding.BI_ERR_NO_DEVICE
+
+
+def test_addmm_bmm_softmax_conv_validation(lib):
+    a, b, c = _t([4, 64]), _t([64, 32]), _t([4, 32])
+    assert lib.bi_addmm(None, _r(a), _r(b), _r(c), None) == binding.BI_ERR_INVALID_ARG
+    assert lib.bi_addmm(_r(_t([31])), _r(a), _r(b), _r(c), None) == binding.BI_ERR_SHAPE_MISMATCH
+    # bmm batch mismatch
+    assert lib.bi_bmm(_r(_t([2, 4, 64])), _r(_t([3, 64, 32])), _r(_t([2, 4, 32], dtype=2)), 1.0,
+                      None) == binding.BI_ERR_SHAPE_MISMATCH
+    # softmax needs fp32 scores
+    assert lib.bi_softmax_lastdim(_r(_t([4, 8])), _r(_t([4, 8])), None) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # conv: output shape must follow the size formula
+    arr = ctypes.c_int32 * 2
+    x, w = _t([2, 3, 224, 224]), _t([1152, 3, 14, 14])
+    bad_y = _t([2, 1152, 15, 16])
+    st = lib.bi_conv2d_patch(_r(x), _r(w), None, _r(bad_y), arr(14, 14), arr(0, 0), arr(1, 1), 1, None)
+    assert st == binding.BI_ERR_SHAPE_MISMATCH
+    # groups must divide the channels
+    st = lib.bi_conv2d_patch(_r(x), _r(w), None, _r(_t([2, 1152, 16, 16])), arr(14, 14), arr(0, 0),
+                             arr(1, 1), 2, None)
+    assert st == binding.BI_ERR_SHAPE_MISMATCH
+    # non-contiguous input
+    xs = _t([2, 3, 224, 224], [3 * 224 * 224, 224 * 224, 1, 224])
+    st = lib.bi_conv2d_patch(_r(xs), _r(w), None, _r(_t([2, 1152, 16, 16])), arr(14, 14), arr(0, 0),
+                             arr(1, 1), 1, None)
+    assert st == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # debug wait: limit out of range is refused before launching
+    assert lib.bi_debug_expire_wait(10, None) == binding.BI_ERR_INVALID_ARG

@@ -1,0 +1,190 @@
+"""GPU parity of bi_mm / bi_addmm against the fp64 oracle, operand layouts,
+ragged tails, exact integer cases, and bitwise batch invariance / run-to-run
+determinism ("Batch-Invariant Kernel Design: Conv2d and Attention BMM",
+section "The two correctness tests": agreement with a reference within a
+tolerance, and sample 0 alone vs in a batch bit for bit)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_gemm_bi_gb300 import binding, inputs
+from tests.gpu_helpers import bits_equal, check_tolerance, padded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    binding.load()
+    yield
+    assert binding.bi_device_status() == binding.BI_OK
+
+
+def _to_gpu(*ts):
+    return [t.cuda() for t in ts]
+
+
+# -- first: the smallest possible case, exact --------------------------------
+
+def test_single_tile_small_integers_exact():
+    a = inputs.small_int_bf16((8, 64), -3, 3, 1)
+    b = inputs.small_int_bf16((64, 16), -3, 3, 2)
+    ref, _ = oracle.mm(a, b)
+    c = binding.bi_mm(*_to_gpu(a, b))
+    torch.cuda.synchronize()
+    assert np.array_equal(c.cpu().double().numpy(), ref)
+
+
+@pytest.mark.parametrize("b_layout", ["mn", "k"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 24, 40), (128, 256, 64), (129, 264, 72),
+                                   (300, 520, 200), (77, 1000, 1000)])
+def test_small_integers_bit_exact(shape, b_layout):
+    # every partial sum is an integer below 2^24: exact in fp32 in any order,
+    # so the GPU must match the oracle bit for bit (fp32 output)
+    M, N, K = shape
+    a = inputs.small_int_bf16((M, K), -4, 4, 3)
+    bt = inputs.small_int_bf16((N, K), -4, 4, 4)
+    b = bt.t().contiguous() if b_layout == "mn" else bt.t()
+    ref, _ = oracle.mm(a, b)
+    ag = a.cuda()
+    bg = b.contiguous().cuda() if b_layout == "mn" else bt.cuda().t()
+    c = binding.bi_mm(ag, bg)
+    assert np.array_equal(c.cpu().double().numpy(), ref)
+
+
+# -- tolerance on real-valued inputs, every layout and ragged tails ----------
+
+RAGGED = [(1, 128, 256), (3, 136, 72), (31, 264, 200), (130, 392, 520), (257, 128, 64),
+          (64, 520, 1000), (200, 8, 8)]
+
+
+@pytest.mark.parametrize("b_layout", ["mn", "k"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", RAGGED)
+def test_mm_matches_oracle(shape, out_dtype, b_layout):
+    M, N, K = shape
+    a = inputs.normal_bf16((M, K), 1.0, 10)
+    w = inputs.normal_bf16((K, N), 0.05, 11)
+    ref, absum = oracle.mm(a, w)
+    bg = w.cuda() if b_layout == "mn" else w.t().contiguous().cuda().t()
+    c = binding.bi_mm(a.cuda(), bg, out_dtype=out_dtype)
+    check_tolerance(c, ref, absum, f"mm {shape} {out_dtype} {b_layout}")
+
+
+@pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(1, 264, 128), (45, 520, 200), (130, 136, 1024)])
+def test_addmm_matches_oracle(shape, bias_dtype):
+    M, N, K = shape
+    x = inputs.normal_bf16((M, K), 1.0, 12)
+    w = inputs.normal_bf16((K, N), 0.02, 13)
+    bias = inputs.normal_bf16((N,), 0.01, 14)
+    ref, absum = oracle.mm(x, w, bias=bias)
+    if bias_dtype == torch.float32:
+        bias_g = bias.float().cuda()   # same values, fp32 storage
+    else:
+        bias_g = bias.cuda()
+    for out_dtype in (torch.bfloat16, torch.float32):
+        c = binding.bi_addmm(bias_g, x.cuda(), w.cuda(), out_dtype=out_dtype)
+        check_tolerance(c, ref, absum, f"addmm {shape} {out_dtype}")
+
+
+def test_strided_operands_and_output_stay_in_their_views():
+    M, N, K = 70, 200, 136
+    a = inputs.normal_bf16((M, K), 1.0, 20)
+    w = inputs.normal_bf16((K, N), 0.05, 21)
+    bias = inputs.normal_bf16((N,), 0.01, 22)
+    ref, absum = oracle.mm(a, w, bias=bias)
+    _, ag = padded(M, K, K + 24)
+    ag.copy_(a.cuda())
+    _, wg = padded(K, N, N + 40)
+    wg.copy_(w.cuda())
+    # output view with row stride 256 inside a canary-filled buffer
+    store = torch.full((M + 2, 256), 12345.0, dtype=torch.float32, device="cuda")
+    out = store[1:M + 1, 8:8 + N]
+    bg = torch.empty(N * 3, dtype=torch.bfloat16, device="cuda")
+    bias_view = bg[::3]
+    bias_view.copy_(bias.cuda())
+    binding.bi_addmm(bias_view, ag, wg, out=out)
+    check_tolerance(out, ref, absum, "strided addmm")
+    mask = torch.ones_like(store, dtype=torch.bool)
+    mask[1:M + 1, 8:8 + N] = False
+    assert torch.all(store[mask] == 12345.0), "a write landed outside the output view"
+
+
+def test_empty_and_degenerate_shapes():
+    a = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(64, 32, dtype=torch.bfloat16, device="cuda")
+    assert binding.bi_mm(a, w).shape == (0, 32)
+    # K == 0: an empty reduction gives exactly the bias
+    bias = inputs.normal_bf16((40,), 1.0, 5).cuda()
+    c = binding.bi_addmm(bias, torch.zeros(3, 0, dtype=torch.bfloat16, device="cuda"),
+                         torch.zeros(0, 40, dtype=torch.bfloat16, device="cuda"), out_dtype=torch.float32)
+    assert torch.equal(c, bias.float().expand(3, 40))
+    c = binding.bi_mm(torch.zeros(2, 0, dtype=torch.bfloat16, device="cuda"),
+                      torch.zeros(0, 8, dtype=torch.bfloat16, device="cuda"))
+    assert torch.equal(c, torch.zeros(2, 8, device="cuda"))
+
+
+def test_unsupported_layout_reports_and_leaves_output_untouched():
+    a = torch.zeros(4, 60, dtype=torch.bfloat16, device="cuda")     # row stride 60: not 16-byte
+    w = torch.zeros(60, 32, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((4, 32), 7.0, device="cuda")
+    with pytest.raises(binding.BiError) as ei:
+        binding.bi_mm(a, w, out=out)
+    assert ei.value.status == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert torch.all(out == 7.0)
+
+
+# -- batch invariance --------------------------------------------------------
+
+def test_tiny_workload_row0_invariant_and_exact_rows():
+    # A [M,256] ~N(0,1), W [256,128] ~N(0,0.02), fp32 output, M in {1,2,3,8,31,32,64}
+    a, w = inputs.tiny_mm(64)
+    ref, absum = oracle.mm(a, w)
+    ag, wg = a.cuda(), w.cuda()
+    full = binding.bi_mm(ag, wg)
+    check_tolerance(full, ref, absum, "tiny mm M=64")
+    for M in inputs.TINY_MM_M:
+        c = binding.bi_mm(ag[:M], wg)
+        check_tolerance(c, ref[:M], absum[:M], f"tiny mm M={M}")
+        # every row, not only row 0, is bit-identical to the same row in the M=64 run
+        assert bits_equal(c, full[:M]), f"M={M}"
+
+
+def test_distractor_rows_do_not_touch_row0():
+    K, N = 1024, 520
+    a = inputs.normal_bf16((300, K), 1.0, 30).cuda()
+    w = inputs.normal_bf16((K, N), 0.02, 31).cuda()
+    alone = binding.bi_mm(a[:1], w)
+    for fill in (2.0 ** 100, -(2.0 ** 100), float("nan"), float("inf")):
+        batch = a.clone()
+        batch[1:] = fill
+        c = binding.bi_mm(batch, w)
+        assert bits_equal(c[:1], alone), fill
+
+
+def test_run_to_run_bitwise():
+    # "Unmasking the True Culprit", section "Why Most GPU Kernels Don't Use
+    # Atomic Operations": repeated products of the same inputs are identical.
+    a = inputs.normal_bf16((2048, 2048), 1.0, 40).cuda()
+    w = inputs.normal_bf16((2048, 2048), 1.0, 41).cuda()
+    ref = binding.bi_mm(a, w)
+    for _ in range(50):
+        assert bits_equal(binding.bi_mm(a, w), ref)
+
+
+def test_linspace_batch_vs_single_row():
+    # the page's structured example: mm(a[:1], b) vs mm(a, b)[:1] with
+    # linspace inputs ("Unmasking the True Culprit", section "The Batch
+    # Invariance Problem Revealed")
+    B, D = 2048, 4096
+    a = torch.linspace(-100, 100, B * D).reshape(B, D).to(torch.bfloat16).cuda()
+    b = torch.linspace(-100, 100, D * D).reshape(D, D).to(torch.bfloat16).cuda()
+    out1 = binding.bi_mm(a[:1], b)
+    out2 = binding.bi_mm(a, b)[:1]
+    assert bits_equal(out1, out2)
+    ref, absum = oracle.mm(a[:1].cpu(), b.cpu())
+    check_tolerance(out1, ref, absum, "linspace row 0")
