@@ -19,6 +19,12 @@ constexpr int kBN = BI_TILE_N;  // UMMA N: output columns per tile
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kUmmaK = 16;      // K per tcgen05.mma (kind::f16)
 constexpr int kGroupM = 16;     // raster group height (L2 reuse only; no numerical effect)
+#ifndef BI_PREFETCH_KBLOCKS
+#define BI_PREFETCH_KBLOCKS 0
+#endif
+// How many K blocks ahead of the shared-memory ring the producer prefetches
+// operand tiles into L2 (0 = off).  A memory-system hint only.
+constexpr int kPrefetchKBlocks = BI_PREFETCH_KBLOCKS;
 
 // Device status codes (the status word holds the first failure of a device).
 // Low byte: a bi_status value; next byte: where it happened.

@@ -111,6 +111,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           } else {
             tma_load_3d(b_dst, &p.tma_b, fb, kb * kBK, tc.nb * kBN, tc.l);
           }
+          if (kPrefetchKBlocks > 0 && kb + kPrefetchKBlocks < p.k_blocks) {
+            const int kp = (kb + kPrefetchKBlocks) * kBK;
+            tma_prefetch_l2_3d(&p.tma_a, kp, tc.mb * kBM, tc.l);
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < kBN / 64; ++j)
+                tma_prefetch_l2_3d(&p.tma_b, tc.nb * kBN + j * 64, kp, tc.l);
+            } else {
+              tma_prefetch_l2_3d(&p.tma_b, kp, tc.nb * kBN, tc.l);
+            }
+          }
           ++it;
         }
       }
