@@ -301,17 +301,22 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
         return {"us": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
                 "gbs": round(nbytes / t / 1e9, 1), "roofline_frac": round(frac, 3), "bound": bound}
 
-    # large square mm, fp32 out
+    # large square mm, fp32 out; plain weight and packed weight
     a, w = inputs.square_mm(max(inputs.SQUARE_MM_M), device="cuda")
+    wp = binding.bi_pack_weight(w)
     rows0 = {}
     res = []
     for M in inputs.SQUARE_MM_M:
         am = a[:M]
         c = torch.empty(M, 8192, dtype=torch.float32, device="cuda")
+        cp = torch.empty(M, 8192, dtype=torch.float32, device="cuda")
         t = measure(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
+        tp = measure(lambda: binding.bi_addmm_packed(None, am, wp, out=cp), flush_buf, stream, reps)
         rows0[M] = c[:1].clone()
         flops, nb = 2.0 * M * 8192 * 8192, 2.0 * (M * 8192 + 8192 * 8192) + 4.0 * M * 8192
-        r = {"M": M, **point(flops, nb, t)}
+        r = {"M": M, **point(flops, nb, t),
+             "packed_weight": {**point(flops, nb, tp), "bits_equal_plain": bits_equal(c, cp)}}
+        del cp
         cb = torch.empty(M, 8192, dtype=torch.bfloat16, device="cuda")
         tc = measure(lambda: torch.mm(am, w, out=cb), flush_buf, stream, reps)
         r["cublas_us_bf16_out"] = round(tc * 1e6, 2)
@@ -323,7 +328,7 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
                         "row0_bit_equal_all_M": all(bits_equal(rows0[M], ref0) for M in inputs.SQUARE_MM_M),
                         "cublas_row0_bit_equal_all_M": all(bits_equal(rows0[("cublas", M)], rows0[("cublas", 1)])
                                                            for M in inputs.SQUARE_MM_M)}
-    del a, w
+    del a, w, wp
 
     # patch-embedding conv
     x, wc, bc = inputs.patch_embed(max(inputs.PATCH_EMBED_B), device="cuda")
@@ -399,19 +404,37 @@ def run_ours(args, rank, local, world):
 
     x, w, bias = inputs.llm_addmm(M_max, device="cuda")
     outs = {M: torch.empty(M, N_DIM, dtype=torch.bfloat16, device="cuda") for M in Ms}
+    outs_other = {M: torch.empty(M, N_DIM, dtype=torch.bfloat16, device="cuda") for M in Ms}
     xs = {M: x[:M] for M in Ms}
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    # The weight is constant: its packed form is made once, outside any timed region.
+    packed = binding.bi_pack_weight(w)
+    torch.cuda.synchronize()
+
+    def launch_packed(M, out):
+        binding.bi_addmm_packed(bias, xs[M], packed, out=out)
+
+    def launch_plain(M, out):
+        binding.bi_addmm(bias, xs[M], w, out=out)
+
+    main_fn, other_fn = ((launch_packed, launch_plain) if args.weight == "packed"
+                         else (launch_plain, launch_packed))
 
     def launch(M):
-        binding.bi_addmm(bias, xs[M], w, out=outs[M])
+        main_fn(M, outs[M])
 
     # warm-up steps
     for _ in range(args.warmup):
         for M in Ms:
             launch(M)
+    for M in Ms:
+        other_fn(M, outs_other[M])
     torch.cuda.synchronize()
-    # row-0 invariance across the sweep (checked on the warm-up outputs)
+    # row-0 invariance across the sweep (checked on the warm-up outputs), and
+    # the packed and plain weights giving the same bits
     row0_equal = all(bits_equal(outs[M][:1], outs[Ms[0]][:1]) for M in Ms)
+    packed_equals_plain = all(bits_equal(outs[M], outs_other[M]) for M in Ms)
+    del outs_other
 
     # timed region: K steps x one launch per M, each after an L2 flush
     events = {M: [] for M in Ms}
@@ -441,6 +464,14 @@ def run_ours(args, rank, local, world):
                       "gbs": round(addmm_bytes(M) / t / 1e9, 1), "roofline_frac": round(frac, 3),
                       "bound": bound})
 
+    # the other weight path, same shapes
+    other_out = {M: torch.empty(M, N_DIM, dtype=torch.bfloat16, device="cuda") for M in Ms}
+    other_name = "plain_weight_us" if args.weight == "packed" else "packed_weight_us"
+    for r in sweep:
+        M = r["M"]
+        r[other_name] = round(measure(lambda: other_fn(M, other_out[M]), flush_buf, stream, 5) * 1e6, 2)
+    del other_out
+
     # cuBLAS on the same sweep (not invariant in general): time + row-0 flag
     cublas_row0 = None
     if not args.no_compare:
@@ -459,7 +490,8 @@ def run_ours(args, rank, local, world):
     roof = {"bound": "tensor", "achieved": round(f_dom / t_dom / 1e12, 2),
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(f_dom / t_dom / 1e12 / peaks["bf16_tflops"], 4),
-            "traffic": traffic, "kernel": "gemm_kernel<MN-major B> (bi_addmm, M=8192)",
+            "traffic": traffic,
+            "kernel": f"gemm_kernel<MN-major B, {args.weight} weight> (bi_addmm{'_packed' if args.weight == 'packed' else ''}, M=8192)",
             "peak_source": f"{peaks['source']} bf16 dense (burst)",
             "algorithmic_bytes": addmm_bytes(M_max)}
 
@@ -468,12 +500,16 @@ def run_ours(args, rank, local, world):
     e2e = None
     if not args.no_compare:
         x_h = x.cpu().pin_memory()
-        w_h = w.cpu().pin_memory()
+        w_src = packed.buffer if args.weight == "packed" else w
+        w_h = w_src.cpu().pin_memory()
         b_h = bias.cpu().pin_memory()
         outs_h = {M: torch.empty(M, N_DIM, dtype=torch.bfloat16).pin_memory() for M in Ms}
         xd = torch.empty_like(x)
-        wd = torch.empty_like(w)
+        wd = torch.empty_like(w_src)
         bd = torch.empty_like(bias)
+        packed_d = binding.PackedWeight(wd, binding.BiPackedWeightDesc(
+            wd.data_ptr(), packed.desc.bytes, packed.desc.K, packed.desc.N, packed.desc.layout,
+            packed.desc.tile_n))
         e2e_steps = max(1, min(args.steps, 5))
 
         def e2e_step():
@@ -481,7 +517,10 @@ def run_ours(args, rank, local, world):
                 xd[:M].copy_(x_h[:M], non_blocking=True)
                 wd.copy_(w_h, non_blocking=True)
                 bd.copy_(b_h, non_blocking=True)
-                binding.bi_addmm(bd, xd[:M], wd, out=outs[M])
+                if args.weight == "packed":
+                    binding.bi_addmm_packed(bd, xd[:M], packed_d, out=outs[M])
+                else:
+                    binding.bi_addmm(bd, xd[:M], wd, out=outs[M])
                 outs_h[M].copy_(outs[M], non_blocking=True)
 
         e2e_step()
@@ -495,7 +534,7 @@ def run_ours(args, rank, local, world):
         torch.cuda.synchronize()
         e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world)
         e2e_val = sum_over_ranks(flops_step * e2e_steps, world) / e2e_s / 1e12
-        h2d = sum(2 * (M * K_DIM + K_DIM * N_DIM + N_DIM) for M in Ms)
+        h2d = sum(2 * (M * K_DIM + N_DIM) + w_src.numel() * w_src.element_size() for M in Ms)
         d2h = sum(2 * M * N_DIM for M in Ms)
         e2e = {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps}
@@ -515,10 +554,14 @@ def run_ours(args, rank, local, world):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "M_sweep": Ms, "K": K_DIM, "N": N_DIM,
                            "out_dtype": "bf16", "accumulate": "fp32",
+                           "weight": ("packed once with bi_pack_weight before timing (same bits as the "
+                                      "plain [4096,14336] weight)" if args.weight == "packed"
+                                      else "plain row-major [4096,14336]"),
                            "l2": "flushed before every timed launch: 512 MB written then read back (L2 cold and clean)",
                            "timing": "CUDA events around each launch on its stream; flush excluded",
                            "wall_s_timed_region": round(t_wall, 3)},
                 "row0_bit_equal_all_M": row0_equal,
+                "packed_equals_plain_all_M": packed_equals_plain,
                 "cublas_row0_bit_equal_all_M": cublas_row0,
                 "sweep": sweep,
                 "roofline": roof,
@@ -542,6 +585,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
+    ap.add_argument("--weight", choices=["packed", "plain"], default="packed",
+                    help="weight path of the timed step (the other one is measured alongside)")
     ap.add_argument("--m-list", type=str, default=None,
                     help="comma-separated subset of the M sweep (for profiling one launch shape)")
     args = ap.parse_args()

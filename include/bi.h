@@ -136,6 +136,46 @@ bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tenso
 bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream);
 
 /*
+ * Packed weights -- for products whose B operand is a fixed weight streamed
+ * from HBM many times (decode-sized M).  Packing stores B as the exact
+ * sequence of 128-byte-swizzled 64 x 64 shared-memory tile images the kernel
+ * would otherwise assemble with strided TMA loads, ordered [k block][64-column
+ * chunk] and zero-padded to whole output tiles, so one pipeline stage of B is
+ * one contiguous range moved by a single bulk copy.  The tensor core reads the
+ * same shared-memory bytes either way: results with a packed weight are bit
+ * identical to results with the plain weight.  Packing is not one of the
+ * pages' operations; it is a data-layout service for the same product.
+ */
+typedef struct {
+  void* ptr;        /* device buffer holding the packed form (caller-owned) */
+  int64_t bytes;    /* its size in bytes */
+  int64_t K, N;     /* logical shape of the packed [K, N] weight */
+  int32_t layout;   /* 1: images of a row-major [K,N] weight, 2: of a [N,K] (transposed view) */
+  int32_t tile_n;   /* output-tile width the packing was made for (must match the library) */
+} bi_packed_weight;
+
+/* Bytes needed to pack a [K, N] bf16 weight (0 for an empty one). */
+int64_t bi_packed_weight_bytes(int64_t K, int64_t N);
+
+/*
+ * Packs b ([K,N] bf16 on the device, unit stride on N or on K, 16-byte aligned
+ * base and 16-byte multiple other stride) into dst (device, 16-byte aligned,
+ * dst_bytes >= bi_packed_weight_bytes(K, N)); fills *out.  Asynchronous on
+ * `stream`; dst must not be used before the packing has run.
+ */
+bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_bytes, bi_packed_weight* out,
+                         bi_stream stream);
+
+/*
+ * c[m,n] = sum_k a[m,k] * B[k,n] (+ bias[n] when bias is non-NULL with a
+ * non-NULL ptr), B given in packed form.  a: [M,K] bf16 as in bi_mm; c: [M,N]
+ * fp32 or bf16 as in bi_mm; bias: [N] bf16 or fp32.  Same arithmetic, same
+ * bits as bi_mm / bi_addmm on the unpacked weight.
+ */
+bi_status bi_addmm_packed(const bi_tensor* bias, const bi_tensor* a, const bi_packed_weight* b,
+                          const bi_tensor* c, bi_stream stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side status word
  * of the current device: BI_OK, or BI_ERR_TIMEOUT when a kernel's bounded
  * wait ran out since the last call (detail in bi_last_error_message()).

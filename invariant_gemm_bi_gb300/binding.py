@@ -26,6 +26,7 @@ BI_ERR_TIMEOUT = 6
 BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
+            "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
             "bi_last_error_message", "bi_abi_version")
 
@@ -35,6 +36,24 @@ _DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 class BiTensor(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("ndim", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class BiPackedWeightDesc(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("layout", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
+
+
+class PackedWeight:
+    """A weight packed on the device by ``bi_pack_weight``: owns the torch
+    buffer that holds it and the descriptor the library reads."""
+
+    def __init__(self, buffer: torch.Tensor, desc: BiPackedWeightDesc):
+        self.buffer = buffer
+        self.desc = desc
+
+    @property
+    def shape(self):
+        return (int(self.desc.K), int(self.desc.N))
 
 
 class BiError(RuntimeError):
@@ -70,6 +89,11 @@ def load(path: str | None = None):
                 "bi_conv2d_patch": ([ptr, ptr, ptr, ptr, i32x2, i32x2, i32x2, ctypes.c_int32,
                                      ctypes.c_void_p], st),
                 "bi_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
+                "bi_packed_weight_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
+                "bi_pack_weight": ([ptr, ctypes.c_void_p, ctypes.c_int64,
+                                    ctypes.POINTER(BiPackedWeightDesc), ctypes.c_void_p], st),
+                "bi_addmm_packed": ([ptr, ptr, ctypes.POINTER(BiPackedWeightDesc), ptr,
+                                     ctypes.c_void_p], st),
                 "bi_device_status": ([ctypes.c_void_p], st),
                 "bi_debug_expire_wait": ([ctypes.c_uint64, ctypes.c_void_p], st),
                 "bi_status_string": ([st], ctypes.c_char_p),
@@ -191,6 +215,37 @@ def bi_softmax_lastdim(s: torch.Tensor, out: torch.Tensor | None = None,
         out = torch.empty(s.shape, dtype=out_dtype, device=s.device)
     ds, dp = _desc(s, "s"), _desc(out, "out")
     _check(lib, "bi_softmax_lastdim", lib.bi_softmax_lastdim(_ref(ds), _ref(dp), _stream(stream)))
+    return out
+
+
+def bi_packed_weight_bytes(K: int, N: int) -> int:
+    return int(load().bi_packed_weight_bytes(int(K), int(N)))
+
+
+def bi_pack_weight(b: torch.Tensor, stream=None) -> PackedWeight:
+    """Packs a [K, N] bf16 weight (row-major, or a transposed view of [N, K])."""
+    lib = load()
+    K, N = b.shape
+    nbytes = bi_packed_weight_bytes(K, N)
+    buf = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=b.device)
+    desc = BiPackedWeightDesc()
+    db = _desc(b, "b")
+    _check(lib, "bi_pack_weight",
+           lib.bi_pack_weight(_ref(db), ctypes.c_void_p(buf.data_ptr()), nbytes, ctypes.byref(desc),
+                              _stream(stream)))
+    return PackedWeight(buf, desc)
+
+
+def bi_addmm_packed(bias: torch.Tensor | None, a: torch.Tensor, b: PackedWeight,
+                    out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.bfloat16,
+                    stream=None) -> torch.Tensor:
+    """out = a @ B (+ bias) with B packed; bit-identical to bi_mm / bi_addmm on the plain weight."""
+    lib = load()
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype, device=a.device)
+    dbias, da, dc = _desc(bias, "bias"), _desc(a, "a"), _desc(out, "out")
+    _check(lib, "bi_addmm_packed",
+           lib.bi_addmm_packed(_ref(dbias), _ref(da), ctypes.byref(b.desc), _ref(dc), _stream(stream)))
     return out
 
 

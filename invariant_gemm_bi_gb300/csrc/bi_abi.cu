@@ -29,7 +29,7 @@ struct DevState {
   std::string why;
   int num_sms = 0;
   unsigned int* status_word = nullptr;
-  bool smem_set[8] = {};
+  bool smem_set[16] = {};
 };
 DevState g_dev[kMaxDevices];
 
@@ -90,9 +90,10 @@ bi_status current_device_info(DeviceInfo* info, std::string* why) {
   return BI_OK;
 }
 
-bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides_bytes, const cuuint32_t* box,
-                       const cuuint32_t* elem_strides, std::string* why) {
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+                  void* ptr, uint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                  const cuuint32_t* box, std::string* why) {
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode_tried) {
@@ -110,14 +111,31 @@ bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint6
     *why = "cuTensorMapEncodeTiled is not available from the driver";
     return false;
   }
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, ptr, dims, strides_bytes, box,
-                        elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(map, dtype, rank, ptr, dims, strides_bytes, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
     return false;
   }
   return true;
+}
+
+bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M, int64_t N,
+                       int64_t ldc, int64_t c_batch) {
+  const uint64_t esz = f32 ? 4 : 2;
+  const uint64_t row = (uint64_t)ldc * esz;
+  const uint64_t bat = L > 1 ? (uint64_t)c_batch * esz : round_up_u64(row * (uint64_t)M, 16);
+  if (reinterpret_cast<uintptr_t>(c) % 16 != 0 || row % 16 != 0 || bat % 16 != 0 || row == 0 ||
+      bat == 0 || M > INT32_MAX || N > INT32_MAX || L > INT32_MAX)
+    return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)L};
+  const cuuint64_t strides[2] = {row, bat};
+  const cuuint32_t box[3] = {32, 32, 1};
+  std::string why;
+  return encode_tiled(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, c, 3, dims,
+                      strides, box, &why);
 }
 
 cudaError_t set_smem_once(const void* func, int bytes, int slot) {
@@ -168,12 +186,6 @@ bi_status check_tensor(const bi_tensor* t, const char* name, int ndim, std::stri
   return BI_OK;
 }
 
-int64_t numel(const bi_tensor* t) {
-  int64_t n = 1;
-  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
-  return n;
-}
-
 bi_status need_ptr(const bi_tensor* t, const char* name, std::string* why) {
   if (!t->ptr) {
     *why = std::string(name) + ": null data pointer";
@@ -191,12 +203,52 @@ bool is_contiguous(const bi_tensor* t) {
   return true;
 }
 
-// Shared by mm / addmm (batched = false) and bmm (batched = true).
+// B: unit stride on N (MN-major) or on K (K-major, a transposed view);
+// 16-byte aligned base, 16-byte multiple non-unit strides.
+bi_status normalize_b(const bi_tensor* b, int o, int64_t L, int64_t K, int64_t N, bool batched,
+                      GemmProblem* g, std::string* why) {
+  const bool mn_ok = (N == 1) || b->stride[o + 1] == 1;
+  const bool k_ok = (K == 1) || b->stride[o] == 1;
+  g->b = b->ptr;
+  g->b_batch = batched ? b->stride[0] : 0;
+  if (mn_ok && (N > 1 || !k_ok)) {
+    g->b_mn_major = 1;
+    g->ldb = (K == 1) ? (int64_t)round_up_u64((uint64_t)N, 8) : b->stride[o];
+  } else if (k_ok) {
+    g->b_mn_major = 0;
+    g->ldb = (N == 1) ? (int64_t)round_up_u64((uint64_t)K, 8) : b->stride[o + 1];
+  } else {
+    *why = "b needs a unit stride on N or on K";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  if (!aligned(b->ptr, 16) || (g->ldb * 2) % 16 != 0 || g->ldb == 0 ||
+      (L > 1 && ((g->b_batch * 2) % 16 != 0 || g->b_batch == 0))) {
+    *why = "b: base must be 16-byte aligned and its non-unit strides multiples of 8 elements";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  return BI_OK;
+}
+
+// Shared by mm / addmm (batched = false) and bmm (batched = true); with
+// `packed`, B comes from a packed weight instead of the tensor b.
 bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor* b,
                       const bi_tensor* c, float alpha, bool batched, cudaStream_t stream,
-                      std::string* why) {
+                      std::string* why, const bi_packed_weight* packed = nullptr) {
   const int nd = batched ? 3 : 2;
   bi_status st;
+  // A packed weight stands in for b as a [K, N] bf16 operand.
+  bi_tensor pb;
+  if (packed) {
+    memset(&pb, 0, sizeof(pb));
+    pb.ptr = packed->ptr;
+    pb.ndim = 2;
+    pb.dtype = BI_BF16;
+    pb.shape[0] = packed->K;
+    pb.shape[1] = packed->N;
+    pb.stride[0] = packed->N;
+    pb.stride[1] = 1;
+    b = &pb;
+  }
   if ((st = check_tensor(a, "a", nd, why)) != BI_OK) return st;
   if ((st = check_tensor(b, "b", nd, why)) != BI_OK) return st;
   if ((st = check_tensor(c, "c", nd, why)) != BI_OK) return st;
@@ -291,27 +343,24 @@ bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor
     *why = "a: base must be 16-byte aligned and its row / batch strides multiples of 8 elements";
     return BI_ERR_UNSUPPORTED_LAYOUT;
   }
-  // B: unit stride on N (MN-major) or on K (K-major, a transposed view).
-  const bool mn_ok = (N == 1) || b->stride[o + 1] == 1;
-  const bool k_ok = (K == 1) || b->stride[o] == 1;
-  g.b = b->ptr;
-  g.b_batch = batched ? b->stride[0] : 0;
-  if (mn_ok && (N > 1 || !k_ok)) {
-    g.b_mn_major = 1;
-    g.ldb = (K == 1) ? (int64_t)round_up_u64((uint64_t)N, 8) : b->stride[o];
-  } else if (k_ok) {
-    g.b_mn_major = 0;
-    g.ldb = (N == 1) ? (int64_t)round_up_u64((uint64_t)K, 8) : b->stride[o + 1];
-  } else {
-    *why = "b needs a unit stride on N or on K";
-    return BI_ERR_UNSUPPORTED_LAYOUT;
+  if (packed) {
+    if (packed->layout != 1 && packed->layout != 2) {
+      *why = "packed weight: unknown layout";
+      return BI_ERR_INVALID_ARG;
+    }
+    if (packed->tile_n != kBN) {
+      *why = "packed weight was made for another tile width";
+      return BI_ERR_INVALID_ARG;
+    }
+    if (!aligned(packed->ptr, 16) || packed->bytes < packed_bytes(K, N)) {
+      *why = "packed weight: buffer not 16-byte aligned or too small";
+      return BI_ERR_INVALID_ARG;
+    }
+    g.b_packed = packed->ptr;
+    g.b_mn_major = packed->layout == 1;
+    return launch_gemm(g, stream, why);
   }
-  if (!aligned(b->ptr, 16) || (g.ldb * 2) % 16 != 0 || g.ldb == 0 ||
-      (L > 1 && ((g.b_batch * 2) % 16 != 0 || g.b_batch == 0))) {
-    *why = "b: base must be 16-byte aligned and its non-unit strides multiples of 8 elements";
-    return BI_ERR_UNSUPPORTED_LAYOUT;
-  }
-  (void)numel;
+  if ((st = normalize_b(b, o, L, K, N, batched, &g, why)) != BI_OK) return st;
   return launch_gemm(g, stream, why);
 }
 
@@ -347,6 +396,49 @@ extern "C" bi_status bi_bmm(const bi_tensor* a, const bi_tensor* b, const bi_ten
                             float alpha, bi_stream stream) {
   std::string why;
   bi_status st = matmul_impl(nullptr, a, b, c, alpha, true, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+extern "C" int64_t bi_packed_weight_bytes(int64_t K, int64_t N) { return packed_bytes(K, N); }
+
+extern "C" bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_bytes,
+                                    bi_packed_weight* out, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if ((st = check_tensor(b, "b", 2, &why)) != BI_OK) return finish(st, why);
+  if (b->dtype != BI_BF16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "b must be bf16");
+  if (!out) return finish(BI_ERR_INVALID_ARG, "out: null");
+  const int64_t K = b->shape[0], N = b->shape[1];
+  if (K == 0 || N == 0) return finish(BI_ERR_INVALID_ARG, "empty weight");
+  const int64_t need = packed_bytes(K, N);
+  if (!dst || !aligned(dst, 16) || dst_bytes < need)
+    return finish(BI_ERR_INVALID_ARG, "dst must be 16-byte aligned with at least " +
+                                          std::to_string(need) + " bytes");
+  if (!b->ptr) return finish(BI_ERR_INVALID_ARG, "b: null data pointer");
+  GemmProblem g;
+  memset(&g, 0, sizeof(g));
+  g.L = 1;
+  g.K = K;
+  g.N = N;
+  if ((st = normalize_b(b, 0, 1, K, N, false, &g, &why)) != BI_OK) return finish(st, why);
+  st = launch_pack(g, dst, (cudaStream_t)stream, &why);
+  if (st == BI_OK) {
+    out->ptr = dst;
+    out->bytes = dst_bytes;
+    out->K = K;
+    out->N = N;
+    out->layout = g.b_mn_major ? 1 : 2;
+    out->tile_n = kBN;
+  }
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_addmm_packed(const bi_tensor* bias, const bi_tensor* a,
+                                     const bi_packed_weight* b, const bi_tensor* c,
+                                     bi_stream stream) {
+  std::string why;
+  if (!b || !b->ptr) return finish(BI_ERR_INVALID_ARG, "packed weight: null");
+  const bi_status st = matmul_impl(bias, a, nullptr, c, 1.0f, false, (cudaStream_t)stream, &why, b);
   return finish(st, why);
 }
 
@@ -509,4 +601,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 1; }
+extern "C" int32_t bi_abi_version(void) { return 2; }

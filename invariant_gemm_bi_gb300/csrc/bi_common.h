@@ -19,12 +19,13 @@ constexpr int kBN = BI_TILE_N;  // UMMA N: output columns per tile
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kUmmaK = 16;      // K per tcgen05.mma (kind::f16)
 constexpr int kGroupM = 16;     // raster group height (L2 reuse only; no numerical effect)
-#ifndef BI_PREFETCH_KBLOCKS
-#define BI_PREFETCH_KBLOCKS 0
-#endif
-// How many K blocks ahead of the shared-memory ring the producer prefetches
-// operand tiles into L2 (0 = off).  A memory-system hint only.
-constexpr int kPrefetchKBlocks = BI_PREFETCH_KBLOCKS;
+constexpr int kShortARows = 32; // A rows staged per k block when M <= 32 (same instructions)
+// Packed weights: B is stored as the sequence of 64 x 64 shared-memory tile
+// images the TMA path would produce (8 KB each, 128-byte swizzled), ordered
+// [k block][64-column chunk], the chunk count padded to whole kBN tiles.  One
+// pipeline stage of B is then one contiguous kBN/64 * 8 KB range.
+constexpr int kPackChunk = 64;
+constexpr int kPackChunkBytes = kPackChunk * kBK * 2;
 
 // Device status codes (the status word holds the first failure of a device).
 // Low byte: a bi_status value; next byte: where it happened.
@@ -36,6 +37,7 @@ enum : unsigned int {
   kSiteDrain = 5,
   kSiteDebugWait = 6,
   kSiteConvProducer = 7,
+  kSitePack = 8,
 };
 __host__ __device__ constexpr unsigned int status_code(unsigned int bi_err, unsigned int site) {
   return bi_err | (site << 8);
@@ -44,6 +46,9 @@ __host__ __device__ constexpr unsigned int status_code(unsigned int bi_err, unsi
 struct GemmParams {
   CUtensorMap tma_a;  // A as [L][M][K] bf16, box {64, 128, 1}, 128B swizzle
   CUtensorMap tma_b;  // K-major B as [L][N][K], box {64, BN, 1}; MN-major as [L][K][N], box {64, 64, 1}
+  CUtensorMap tma_c;  // C as [L][M][N], box {32, 32, 1} (fp32: 128B swizzle, bf16: 64B), if use_tma_store
+  const uint8_t* b_packed;   // packed B (see kPackChunk), or null
+  int64_t packed_kb_stride;  // bytes between consecutive k blocks of the packed B
   void* c;
   const void* bias;
   int64_t ldc;             // elements
@@ -55,12 +60,13 @@ struct GemmParams {
   int32_t out_f32;    // 1: fp32 output, 0: bf16 output
   int32_t bias_kind;  // 0: none, 1: bf16, 2: fp32
   int32_t vec_store;  // 1: every output row start is 16-byte aligned
-  int32_t pad_;
+  int32_t use_tma_store;
   unsigned int* status_word;
   uint64_t wait_limit_ns;
 };
 
 struct ConvParams {
+  CUtensorMap tma_y;   // y as [B*groups][Cog][P], box {32, 32, 1}, if use_tma_store
   const uint16_t* x;   // [B][C][H][W] bf16 contiguous
   const uint16_t* w;   // [Co][C/groups][KH][KW] bf16 contiguous
   const void* bias;    // [Co] or null
@@ -70,7 +76,7 @@ struct ConvParams {
   int32_t Cig, Cog, Kg;       // channels per group in/out, reduction length per group
   int32_t P;                  // Ho*Wo output positions per sample
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;  // per (sample, group) tile space
-  int32_t out_f32, bias_kind, vec_store;
+  int32_t out_f32, bias_kind, vec_store, use_tma_store;
   unsigned int* status_word;
   uint64_t wait_limit_ns;
 };

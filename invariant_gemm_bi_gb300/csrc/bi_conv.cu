@@ -28,9 +28,9 @@ struct ConvLayout {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int MAX_DYN = 232448;
-  static constexpr int FIT = (MAX_DYN - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int FIT = (MAX_DYN - 1024 - BAR_BYTES - kEpilogueStagingBytes) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-  static constexpr int DYN_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int DYN_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + kEpilogueStagingBytes;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
   static_assert(DYN_BYTES > 116 * 1024, "one CTA per SM: TMEM is allocated whole");
 };
@@ -42,13 +42,6 @@ constexpr int kConvThreads = 288;  // 4 producer warps, 1 MMA warp, 4 epilogue w
 // rows hold 64 bf16 of K: 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
 }
 
 __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_constant__ ConvParams p) {
@@ -176,7 +169,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
   } else if (warp == 4) {
     if (lane == 0)
       mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, false>(sA, sB, bars, tmem_base,
-                                                               p.num_tiles, p.k_blocks, wc);
+                                                               p.num_tiles, p.k_blocks, gridDim.x, wc);
   } else {
     OutDesc o;
     o.c = p.y;
@@ -192,7 +185,10 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
     o.vec_store = p.vec_store;
     o.bias_per_row = 1;
     o.bias_groups = p.groups;
-    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, o, wc);
+    o.tma_c = p.use_tma_store ? &p.tma_y : nullptr;
+    const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 5) * 2 * kStageOutBytes;
+    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, gridDim.x, o,
+                  staging, wc);
   }
 
   tc_fence_before_sync();
@@ -247,10 +243,14 @@ bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* w
   p.bias_kind = cp.bias_kind;
   const int esz = cp.out_f32 ? 4 : 2;
   p.vec_store = ((reinterpret_cast<uintptr_t>(cp.y) % 16) == 0 && ((int64_t)p.P * esz) % 16 == 0) ? 1 : 0;
+  p.use_tma_store = encode_output_map(&p.tma_y, cp.y, cp.out_f32 != 0, cp.B * cp.groups, p.Cog, p.P,
+                                      p.P, (int64_t)p.Cog * p.P)
+                        ? 1
+                        : 0;
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
   const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&conv_kernel), ConvLayout::DYN_BYTES, 2);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&conv_kernel), ConvLayout::DYN_BYTES, 4);
   if (e == cudaSuccess) conv_kernel<<<grid, kConvThreads, ConvLayout::DYN_BYTES, stream>>>(p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {

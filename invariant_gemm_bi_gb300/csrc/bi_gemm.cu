@@ -1,11 +1,15 @@
-// bi_gemm.cu -- persistent, warp-specialised tcgen05 GEMM for mm / addmm / bmm.
+// bi_gemm.cu -- persistent, warp-specialised tcgen05 GEMM for mm / addmm / bmm,
+// and the weight packer.
 //
-//   warp 0      TMA producer: A (128 x 64) and B (kBN x 64) tiles of each K
-//               block into a ring of shared-memory stages (128-byte swizzle,
-//               out-of-range elements zero-filled by the copy engine)
-//   warp 1      TMEM allocator + single-thread UMMA issuer (fp32 accumulator
-//               in TMEM, double-buffered so the epilogue of tile i overlaps
-//               the main loop of tile i+1)
+//   warp 0      producer: A (128 x 64) and B (kBN x 64) tiles of each K block
+//               into a ring of shared-memory stages (128-byte swizzle).  A always
+//               arrives by TMA (out-of-range rows / K zero-filled by the copy
+//               engine).  B arrives either by TMA from its strided layout, or --
+//               for a packed weight -- as one contiguous 1-D bulk copy per stage
+//               of the very same shared-memory image.
+//   warp 1      TMEM allocator + single-thread UMMA issuer (fp32 accumulator in
+//               TMEM, double-buffered so the epilogue of tile i overlaps the main
+//               loop of tile i+1)
 //   warps 2..5  epilogue: tcgen05.ld -> alpha / bias -> rounding -> global
 //
 // Batch elements of bmm are a third tile coordinate, so tiles never straddle
@@ -22,26 +26,81 @@
 
 namespace bi {
 
+// Shared-memory plan of the GEMM.  A_ROWS = 128 is the general layout: A
+// stages hold a whole 128-row A tile, and the epilogue stages its output for
+// TMA stores.  A_ROWS = 32 is the short-A layout for problems with at most 32
+// rows (decode-sized M), where the weight stream is the whole cost: A stages
+// hold 32 rows, which frees room for more B stages in flight.  The tensor core
+// still runs the same 128 x kBN x 16 instructions in the same K order; its A
+// rows 32..127 read whatever lies beyond the 32-row stage and only produce
+// accumulator rows that are never stored (no output row reads another row's
+// A data), so every stored element is computed exactly as in the general layout.
+template <int A_ROWS>
 struct GemmLayout {
-  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int A_BYTES = A_ROWS * kBK * 2;
   static constexpr int B_BYTES = kBN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 1024;
+  static constexpr int STAGING_BYTES = A_ROWS == kBM ? kEpilogueStagingBytes : 0;
+  // The UMMA reads up to 128 A rows from each stage's A base: keep that span
+  // inside the allocation for the last A stage.
+  static constexpr int A_OVERREAD = (kBM - A_ROWS) * kBK * 2;
   static constexpr int MAX_DYN = 232448;  // 227 KB, the opt-in per-block maximum
-  static constexpr int FIT = (MAX_DYN - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int FIT = (MAX_DYN - 1024 - BAR_BYTES - STAGING_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-  static constexpr int DYN_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int DYN_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + STAGING_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
   static_assert(DYN_BYTES > 116 * 1024, "one CTA per SM: TMEM is allocated whole");
+  static_assert(B_BYTES == (kBN / kPackChunk) * kPackChunkBytes, "packed stage = whole chunks");
+  static_assert(A_OVERREAD <= STAGES * B_BYTES, "A over-read stays inside the B stages");
 };
 
 constexpr int kGemmThreads = 192;
 
-template <bool B_MN>
+// Producer cursor over this CTA's (tile, k block) sequence.
+struct ProdCursor {
+  int tile, kb;
+  uint32_t it;
+  TileCoord tc;  // coordinates of `tile` (decoded once per tile)
+};
+
+template <bool B_MN, bool B_PACKED, int A_ROWS>
+__device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, uint32_t sB,
+                                            const PipeBars& bars, const ProdCursor& c) {
+  using Lay = GemmLayout<A_ROWS>;
+  const uint32_t s = c.it % Lay::STAGES;
+  const TileCoord& tc = c.tc;
+  const uint32_t fb = bars.full(s);
+  mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
+  tma_load_3d(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
+  const uint32_t b_dst = sB + s * Lay::B_BYTES;
+  if (B_PACKED) {
+    const uint8_t* src = p.b_packed + (int64_t)c.kb * p.packed_kb_stride + (int64_t)tc.nb * Lay::B_BYTES;
+    bulk_load(b_dst, src, Lay::B_BYTES, fb);
+  } else if (B_MN) {
+#pragma unroll
+    for (int j = 0; j < kBN / 64; ++j)
+      tma_load_3d(b_dst + j * 8192, &p.tma_b, fb, tc.nb * kBN + j * 64, c.kb * kBK, tc.l);
+  } else {
+    tma_load_3d(b_dst, &p.tma_b, fb, c.kb * kBK, tc.nb * kBN, tc.l);
+  }
+}
+
+__device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int stride) {
+  ++c.it;
+  if (++c.kb == p.k_blocks) {
+    c.kb = 0;
+    c.tile += stride;
+    if (c.tile < p.num_tiles) c.tc = decode_tile(c.tile, p.m_tiles, p.n_tiles);
+  }
+}
+
+template <bool B_MN, bool B_PACKED, int A_ROWS>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Lay = GemmLayout;
+  using Lay = GemmLayout<A_ROWS>;
+  const int stride = gridDim.x;  // grid = min(#tiles, #SMs): every CTA owns tiles
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -60,6 +119,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  ProdCursor cur{(int)blockIdx.x, 0, 0u, {0, 0, 0}};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Lay::STAGES; ++s) {
@@ -73,6 +133,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // The first ring's worth of loads needs no free-stage wait: start the
+    // memory traffic before the rest of the CTA is set up.
+    tma_prefetch_desc(&p.tma_a);
+    if (!B_PACKED) tma_prefetch_desc(&p.tma_b);
+    cur.tc = decode_tile(cur.tile, p.m_tiles, p.n_tiles);
+    while (cur.it < (uint32_t)Lay::STAGES && cur.tile < p.num_tiles) {
+      issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur);
+      advance(cur, p, stride);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
@@ -86,47 +155,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&p.tma_a);
-      tma_prefetch_desc(&p.tma_b);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const TileCoord tc = decode_tile(tile, p.m_tiles, p.n_tiles);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          const uint32_t s = it % Lay::STAGES;
-          const uint32_t r = it / Lay::STAGES;
-          if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
-                                          wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = bars.full(s);
-          mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
-          tma_load_3d(sA + s * Lay::A_BYTES, &p.tma_a, fb, kb * kBK, tc.mb * kBM, tc.l);
-          const uint32_t b_dst = sB + s * Lay::B_BYTES;
-          if (B_MN) {
-#pragma unroll
-            for (int j = 0; j < kBN / 64; ++j)
-              tma_load_3d(b_dst + j * 8192, &p.tma_b, fb, tc.nb * kBN + j * 64, kb * kBK, tc.l);
-          } else {
-            tma_load_3d(b_dst, &p.tma_b, fb, kb * kBK, tc.nb * kBN, tc.l);
-          }
-          if (kPrefetchKBlocks > 0 && kb + kPrefetchKBlocks < p.k_blocks) {
-            const int kp = (kb + kPrefetchKBlocks) * kBK;
-            tma_prefetch_l2_3d(&p.tma_a, kp, tc.mb * kBM, tc.l);
-            if (B_MN) {
-#pragma unroll
-              for (int j = 0; j < kBN / 64; ++j)
-                tma_prefetch_l2_3d(&p.tma_b, tc.nb * kBN + j * 64, kp, tc.l);
-            } else {
-              tma_prefetch_l2_3d(&p.tma_b, kp, tc.nb * kBN, tc.l);
-            }
-          }
-          ++it;
-        }
+      while (cur.tile < p.num_tiles) {
+        const uint32_t s = cur.it % Lay::STAGES;
+        const uint32_t r = cur.it / Lay::STAGES;  // >= 1 here
+        if (!mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word, wc.limit_ns,
+                               status_code(6, kSiteProducerEmpty)))
+          break;
+        issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur);
+        advance(cur, p, stride);
       }
       // No copy may still be landing in shared memory when the CTA exits:
       // wait (bounded) for the last fill of every stage.
+      const uint32_t it = cur.it;
       const uint32_t first = it > (uint32_t)Lay::STAGES ? it - Lay::STAGES : 0u;
       for (uint32_t j = first; j < it; ++j)
         mbar_wait_bounded(bars.full(j % Lay::STAGES), (j / Lay::STAGES) & 1, nullptr,
@@ -135,7 +175,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   } else if (warp == 1) {
     if (lane == 0)
       mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, B_MN>(sA, sB, bars, tmem_base, p.num_tiles,
-                                                              p.k_blocks, wc);
+                                                              p.k_blocks, stride, wc);
   } else {
     OutDesc o;
     o.c = p.c;
@@ -151,7 +191,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     o.vec_store = p.vec_store;
     o.bias_per_row = 0;
     o.bias_groups = 1;
-    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, o, wc);
+    o.tma_c = (Lay::STAGING_BYTES > 0 && p.use_tma_store) ? &p.tma_c : nullptr;
+    const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 2) * 2 * kStageOutBytes;
+    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, stride, o,
+                  staging, wc);
   }
 
   tc_fence_before_sync();
@@ -164,6 +207,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
+// Weight packer: chunk c = (k block kb, 64-column chunk nc) of the packed
+// buffer receives, byte for byte, the 64 x 64 shared-memory image that the
+// GEMM's TMA path would load for it (same tensor map geometry, same swizzle,
+// zeros outside the matrix).  One warp per CTA: TMA load -> smem -> bulk store.
+// ---------------------------------------------------------------------------
+constexpr int kPackThreads = 32;
+constexpr int kPackDynBytes = 1024 + kPackChunkBytes + 64;
+
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                            uint8_t* dst, int k_blocks, int nc_pad,
+                                                            int b_mn, unsigned int* status_word,
+                                                            uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t buf = (raw + 1023u) & ~1023u;
+  const uint32_t bar = buf + kPackChunkBytes;
+  int* abort_flag = reinterpret_cast<int*>(smem_raw + (bar + 8 - raw));
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap);
+    uint32_t phase = 0;
+    const int64_t total = (int64_t)k_blocks * nc_pad;
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
+      const int kb = (int)(c / nc_pad);
+      const int nc = (int)(c - (int64_t)kb * nc_pad);
+      mbar_arrive_expect_tx(bar, kPackChunkBytes);
+      if (b_mn)
+        tma_load_3d(buf, &tmap, bar, nc * kPackChunk, kb * kBK, 0);
+      else
+        tma_load_3d(buf, &tmap, bar, kb * kBK, nc * kPackChunk, 0);
+      if (!mbar_wait_bounded(bar, phase, abort_flag, status_word, limit_ns,
+                             status_code(6, kSitePack)))
+        break;
+      phase ^= 1u;
+      bulk_store(dst + c * kPackChunkBytes, buf, kPackChunkBytes);
+      bulk_commit();
+      bulk_wait_read_all();  // the buffer is refilled next iteration
+    }
+    bulk_wait_all();
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -173,8 +262,69 @@ static bool encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
   const cuuint32_t box[3] = {b0, b1, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return encode_tiled_bf16(map, const_cast<void*>(ptr), 3, dims, strides, box, estr, why);
+  return encode_tiled_bf16(map, const_cast<void*>(ptr), 3, dims, strides, box, why);
+}
+
+// B's tensor map: MN-major as [L][K][N] with 64 x 64 boxes, K-major as
+// [L][N][K] with 64 x rows boxes.
+static bool encode_b(CUtensorMap* map, const GemmProblem& g, uint32_t k_major_rows, std::string* why) {
+  const uint64_t b_row = (uint64_t)g.ldb * 2;
+  if (g.b_mn_major) {
+    const uint64_t b_bat = g.L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)g.K, 16);
+    return encode_3d(map, g.b, g.N, g.K, g.L, b_row, b_bat, 64, kBK, why);
+  }
+  const uint64_t b_bat = g.L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)g.N, 16);
+  return encode_3d(map, g.b, g.K, g.N, g.L, b_row, b_bat, kBK, k_major_rows, why);
+}
+
+int64_t packed_bytes(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0) return 0;
+  const int64_t k_blocks = (K + kBK - 1) / kBK;
+  const int64_t n_tiles = (N + kBN - 1) / kBN;
+  return k_blocks * n_tiles * (kBN / kPackChunk) * (int64_t)kPackChunkBytes;
+}
+
+bi_status launch_pack(const GemmProblem& g, void* dst, cudaStream_t stream, std::string* why) {
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, why);
+  if (st != BI_OK) return st;
+  CUtensorMap map;
+  if (!encode_b(&map, g, kPackChunk, why)) return BI_ERR_CUDA;
+  const int k_blocks = (int)((g.K + kBK - 1) / kBK);
+  const int nc_pad = (int)(((g.N + kBN - 1) / kBN) * (kBN / kPackChunk));
+  const int64_t total = (int64_t)k_blocks * nc_pad;
+  const int grid = (int)std::min<int64_t>(total, (int64_t)dev.num_sms * 8);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&pack_kernel), kPackDynBytes, 5);
+  if (e == cudaSuccess)
+    pack_kernel<<<grid, kPackThreads, kPackDynBytes, stream>>>(map, reinterpret_cast<uint8_t*>(dst),
+                                                               k_blocks, nc_pad, g.b_mn_major,
+                                                               dev.status_word, kWaitLimitNs);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("pack launch: ") + cudaGetErrorString(e);
+    return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
+template <bool B_MN, bool B_PACKED, int A_ROWS>
+static cudaError_t launch_variant(const GemmParams& p, int grid, cudaStream_t stream, int slot) {
+  using Lay = GemmLayout<A_ROWS>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gemm_kernel<B_MN, B_PACKED, A_ROWS>),
+                                Lay::DYN_BYTES, slot);
+  if (e == cudaSuccess)
+    gemm_kernel<B_MN, B_PACKED, A_ROWS><<<grid, kGemmThreads, Lay::DYN_BYTES, stream>>>(p);
+  return e;
+}
+
+template <int A_ROWS>
+static cudaError_t launch_rows(const GemmProblem& g, const GemmParams& p, int grid,
+                               cudaStream_t stream, int slot0) {
+  if (g.b_packed)
+    return g.b_mn_major ? launch_variant<true, true, A_ROWS>(p, grid, stream, slot0 + 2)
+                        : launch_variant<false, true, A_ROWS>(p, grid, stream, slot0 + 3);
+  return g.b_mn_major ? launch_variant<true, false, A_ROWS>(p, grid, stream, slot0)
+                      : launch_variant<false, false, A_ROWS>(p, grid, stream, slot0 + 1);
 }
 
 bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* why) {
@@ -187,17 +337,17 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   const int64_t L = g.L, M = g.M, N = g.N, K = g.K;
   // A: [L][M][K]; the batch stride of a single batch element is never used,
   // but must still be a legal (16-byte multiple) stride.
+  // Short-A layout when every tile has at most 32 rows (see GemmLayout).
+  const bool short_a = M <= kShortARows;
   const uint64_t a_row = (uint64_t)g.lda * 2;
   const uint64_t a_bat = L > 1 ? (uint64_t)g.a_batch * 2 : round_up_u64(a_row * (uint64_t)M, 16);
-  if (!encode_3d(&p.tma_a, g.a, K, M, L, a_row, a_bat, kBK, kBM, why)) return BI_ERR_CUDA;
-  if (g.b_mn_major) {
-    const uint64_t b_row = (uint64_t)g.ldb * 2;  // stride between k rows
-    const uint64_t b_bat = L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)K, 16);
-    if (!encode_3d(&p.tma_b, g.b, N, K, L, b_row, b_bat, 64, kBK, why)) return BI_ERR_CUDA;
-  } else {
-    const uint64_t b_row = (uint64_t)g.ldb * 2;  // stride between n rows
-    const uint64_t b_bat = L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)N, 16);
-    if (!encode_3d(&p.tma_b, g.b, K, N, L, b_row, b_bat, kBK, kBN, why)) return BI_ERR_CUDA;
+  if (!encode_3d(&p.tma_a, g.a, K, M, L, a_row, a_bat, kBK, short_a ? kShortARows : kBM, why))
+    return BI_ERR_CUDA;
+  if (g.b_packed) {
+    p.b_packed = reinterpret_cast<const uint8_t*>(g.b_packed);
+    p.packed_kb_stride = ((N + kBN - 1) / kBN) * (int64_t)(kBN * kBK * 2);
+  } else if (!encode_b(&p.tma_b, g, kBN, why)) {
+    return BI_ERR_CUDA;
   }
   p.c = g.c;
   p.bias = g.bias;
@@ -221,20 +371,13 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   p.out_f32 = g.out_f32;
   p.bias_kind = g.bias_kind;
   p.vec_store = g.vec_store;
+  p.use_tma_store = encode_output_map(&p.tma_c, g.c, g.out_f32 != 0, L, M, N, g.ldc, g.c_batch) ? 1 : 0;
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
 
   const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
-  cudaError_t e;
-  if (g.b_mn_major) {
-    e = set_smem_once(reinterpret_cast<const void*>(&gemm_kernel<true>), GemmLayout::DYN_BYTES, 0);
-    if (e == cudaSuccess)
-      gemm_kernel<true><<<grid, kGemmThreads, GemmLayout::DYN_BYTES, stream>>>(p);
-  } else {
-    e = set_smem_once(reinterpret_cast<const void*>(&gemm_kernel<false>), GemmLayout::DYN_BYTES, 1);
-    if (e == cudaSuccess)
-      gemm_kernel<false><<<grid, kGemmThreads, GemmLayout::DYN_BYTES, stream>>>(p);
-  }
+  cudaError_t e = short_a ? launch_rows<kShortARows>(g, p, grid, stream, 8)
+                          : launch_rows<kBM>(g, p, grid, stream, 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("gemm launch: ") + cudaGetErrorString(e);

@@ -31,11 +31,23 @@ struct DeviceInfo {
 // BI_ERR_NO_DEVICE unless the device is compute capability 10.3 (sm_103).
 bi_status current_device_info(DeviceInfo* info, std::string* why);
 
-// cuTensorMapEncodeTiled for a bf16 tensor with 128-byte swizzle and zero
-// fill out of bounds (driver entry point resolved once through the runtime).
-bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides_bytes, const cuuint32_t* box,
-                       const cuuint32_t* elem_strides, std::string* why);
+// cuTensorMapEncodeTiled with zero fill out of bounds (driver entry point
+// resolved once through the runtime).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+                  void* ptr, uint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                  const cuuint32_t* box, std::string* why);
+// bf16 operand tiles with the 128-byte swizzle.
+inline bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const cuuint64_t* dims,
+                              const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                              std::string* why) {
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, ptr, rank,
+                      dims, strides_bytes, box, why);
+}
+// Tensor map of an output [L][M][N] (row stride ldc, batch stride c_batch,
+// elements) for the epilogue's 32 x 32 tile stores; false when the layout is
+// not TMA-legal (the epilogue then stores directly).
+bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M, int64_t N,
+                       int64_t ldc, int64_t c_batch);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, slot).
 cudaError_t set_smem_once(const void* func, int bytes, int slot);
@@ -47,6 +59,7 @@ struct GemmProblem {
   const void* b;  // bf16; b_mn_major: b[l][k][n] at k*ldb + n; else at n*ldb + k
   int64_t ldb, b_batch;
   int b_mn_major;
+  const void* b_packed;  // packed weight (L == 1), or null; b_mn_major gives its image layout
   void* c;  // [L][M][N], unit stride on N
   int64_t ldc, c_batch;
   int out_f32;
@@ -59,6 +72,10 @@ struct GemmProblem {
 };
 
 bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* why);
+
+// Bytes of the packed form of a [K, N] weight; packs g's B (L == 1) into dst.
+int64_t packed_bytes(int64_t K, int64_t N);
+bi_status launch_pack(const GemmProblem& g, void* dst, cudaStream_t stream, std::string* why);
 
 struct ConvProblem {
   const void* x;

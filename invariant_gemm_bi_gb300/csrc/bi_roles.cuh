@@ -14,7 +14,8 @@
 //   * the epilogue computes round(acc * alpha + bias) with separately
 //     rounded fp32 multiply and add, then one conversion to the output type.
 // Which CTA takes which tile (the persistent stride and the raster order)
-// changes nothing in that sequence.
+// changes nothing in that sequence.  `stride` is the number of CTAs that own
+// tiles: CTA c takes tiles c, c + stride, c + 2*stride, ...
 #pragma once
 
 #include <cuda_bf16.h>
@@ -65,12 +66,12 @@ struct WaitCtl {
 template <int STAGES, int A_BYTES, int B_BYTES, bool B_MN>
 __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBars& bars,
                                          uint32_t tmem_base, int num_tiles, int k_blocks,
-                                         const WaitCtl& w) {
+                                         int stride, const WaitCtl& w) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, B_MN);
   uint32_t it = 0;
   int local = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += stride, ++local) {
     const uint32_t buf = local & 1;
     const uint32_t use = local >> 1;
     if (use > 0 &&
@@ -114,15 +115,24 @@ __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBar
 //   out[l][m][n] at c + l*c_batch_stride + m*ldc + n,
 //   value = round(acc * alpha (+ bias)), bias either per column n or per
 //   row m (the convolution's output channel, offset by (l % bias_groups)*M).
+// With tma_c set, each warp stages its 32 x 32 chunk in shared memory
+// (swizzled, bank-conflict free) and writes it with a TMA tile store that
+// clips rows >= M and columns >= N; otherwise threads store directly.
 struct OutDesc {
   void* c;
   const void* bias;
+  const CUtensorMap* tma_c;  // tensor map of c as [L][M][N] with 32 x 32 boxes, or null
   int64_t ldc, c_batch_stride, bias_stride;
   float alpha;
   int32_t M, N;
   int32_t out_f32, bias_kind, vec_store;
   int32_t bias_per_row, bias_groups;
 };
+
+// Epilogue staging: per epilogue warp, two 4 KB buffers (double-buffered
+// against the TMA stores in flight), 1 KB aligned.
+constexpr int kStageOutBytes = 4096;
+constexpr int kEpilogueStagingBytes = 4 * 2 * kStageOutBytes;
 
 __device__ __forceinline__ float load_bias(const OutDesc& o, int64_t idx) {
   if (o.bias_kind == 1) {
@@ -132,16 +142,14 @@ __device__ __forceinline__ float load_bias(const OutDesc& o, int64_t idx) {
   return reinterpret_cast<const float*>(o.bias)[idx * o.bias_stride];
 }
 
-// Thread owns output row m and 32 consecutive columns starting at n0.
-__device__ __forceinline__ void store_32(const OutDesc& o, int l, int m, int n0,
-                                         const uint32_t (&v)[32]) {
-  if (m >= o.M || n0 >= o.N) return;
-  float f[32];
+// f = acc * alpha (+ bias), each a separately rounded fp32 operation.
+__device__ __forceinline__ void epilogue_math(const OutDesc& o, int l, int m, int n0,
+                                              const uint32_t (&v)[32], float (&f)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), o.alpha);
   if (o.bias_kind) {
     if (o.bias_per_row) {
-      const float bv = load_bias(o, (int64_t)(l % o.bias_groups) * o.M + m);
+      const float bv = (m < o.M) ? load_bias(o, (int64_t)(l % o.bias_groups) * o.M + m) : 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) f[i] = __fadd_rn(f[i], bv);
     } else {
@@ -150,6 +158,17 @@ __device__ __forceinline__ void store_32(const OutDesc& o, int l, int m, int n0,
         if (n0 + i < o.N) f[i] = __fadd_rn(f[i], load_bias(o, n0 + i));
     }
   }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Thread owns output row m and 32 consecutive columns starting at n0.
+__device__ __forceinline__ void store_32_direct(const OutDesc& o, int l, int m, int n0,
+                                                const float (&f)[32]) {
+  if (m >= o.M || n0 >= o.N) return;
   const int64_t off = (int64_t)l * o.c_batch_stride + (int64_t)m * o.ldc + n0;
   const bool full = o.vec_store && (n0 + 32 <= o.N);
   if (o.out_f32) {
@@ -166,16 +185,11 @@ __device__ __forceinline__ void store_32(const OutDesc& o, int l, int m, int n0,
   } else {
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.c) + off;
     if (full) {
-      uint32_t packed[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-        packed[i] = *reinterpret_cast<uint32_t*>(&h);
-      }
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        d4[i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                           pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -184,13 +198,36 @@ __device__ __forceinline__ void store_32(const OutDesc& o, int l, int m, int n0,
   }
 }
 
+// Lane `lane` writes its row of the warp's 32 x 32 chunk into the staging
+// buffer in the layout of the store's tensor map: fp32 rows of 128 bytes with
+// the 128-byte swizzle, bf16 rows of 64 bytes with the 64-byte swizzle.
+__device__ __forceinline__ void stage_32(const OutDesc& o, uint32_t sbuf, int lane,
+                                         const float (&f)[32]) {
+  if (o.out_f32) {
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+      st_shared_v4(sbuf + lane * 128 + ((cc ^ (lane & 7)) << 4), __float_as_uint(f[4 * cc]),
+                   __float_as_uint(f[4 * cc + 1]), __float_as_uint(f[4 * cc + 2]),
+                   __float_as_uint(f[4 * cc + 3]));
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      st_shared_v4(sbuf + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
+                   pack_bf16x2(f[8 * cc], f[8 * cc + 1]), pack_bf16x2(f[8 * cc + 2], f[8 * cc + 3]),
+                   pack_bf16x2(f[8 * cc + 4], f[8 * cc + 5]), pack_bf16x2(f[8 * cc + 6], f[8 * cc + 7]));
+  }
+}
+
 // One warp of the epilogue group: drains TMEM lane quadrant q (rows
-// 32q .. 32q+31 of each tile) for every tile of this CTA.
+// 32q .. 32q+31 of each tile) for every tile of this CTA.  stage_base: this
+// warp's two staging buffers (used when o.tma_c is set).
 __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_base,
                                               const PipeBars& bars, int num_tiles, int m_tiles,
-                                              int n_tiles, const OutDesc& o, const WaitCtl& w) {
+                                              int n_tiles, int stride, const OutDesc& o,
+                                              uint32_t stage_base, const WaitCtl& w) {
   int local = 0;
-  for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+  uint32_t chunk = 0;  // staged chunks issued by this warp (selects the buffer)
+  for (int tile = blockIdx.x; tile < num_tiles; tile += stride, ++local) {
     const uint32_t buf = local & 1;
     const uint32_t use = local >> 1;
     const bool ok = mbar_wait_bounded(bars.tfull(buf), use & 1, w.abort, w.status_word,
@@ -198,19 +235,44 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after_sync();
     const TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
-    const int m = tc.mb * kBM + q * 32 + lane;
+    const int m0 = tc.mb * kBM + q * 32;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kBN;
 #pragma unroll 1
     for (int j = 0; j < kBN / 32; ++j) {
       uint32_t v[32];
       tmem_load_32cols(lane_addr + j * 32, v);
       tmem_load_wait();
-      store_32(o, tc.l, m, tc.nb * kBN + j * 32, v);
+      const int n0 = tc.nb * kBN + j * 32;
+      float f[32];
+      epilogue_math(o, tc.l, m0 + lane, n0, v, f);
+      if (o.tma_c) {
+        if (n0 < o.N && m0 < o.M) {  // boxes wholly past the matrix are skipped, not issued
+          const uint32_t sbuf = stage_base + (chunk & 1) * kStageOutBytes;
+          if (chunk >= 2) {  // the store issued two chunks ago must have read this buffer
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+          }
+          stage_32(o, sbuf, lane, f);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(o.tma_c, sbuf, n0, m0, tc.l);
+            bulk_commit();
+          }
+          ++chunk;
+        }
+      } else {
+        store_32_direct(o, tc.l, m0 + lane, n0, f);
+      }
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.tempty(buf));
   }
+  // Shared memory must outlive the reads of the stores still in flight, and
+  // the results must be complete when the kernel ends.
+  if (o.tma_c && lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 }  // namespace bi

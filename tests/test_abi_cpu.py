@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 1
+    assert lib.bi_abi_version() == 2
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -148,3 +148,25 @@ def test_addmm_bmm_softmax_conv_validation(lib):
     assert st == binding.BI_ERR_UNSUPPORTED_LAYOUT
     # debug wait: limit out of range is refused before launching
     assert lib.bi_debug_expire_wait(10, None) == binding.BI_ERR_INVALID_ARG
+
+
+def test_packed_weight_size_and_validation(lib):
+    # [k blocks of 64] x [tiles of 256 columns] x 32 KB
+    assert lib.bi_packed_weight_bytes(4096, 14336) == 64 * 56 * 32768
+    assert lib.bi_packed_weight_bytes(65, 257) == 2 * 2 * 32768
+    assert lib.bi_packed_weight_bytes(0, 8) == 0
+    desc = binding.BiPackedWeightDesc()
+    # destination too small
+    st = lib.bi_pack_weight(_r(_t([64, 256])), FAKE, 1024, ctypes.byref(desc), None)
+    assert st == binding.BI_ERR_INVALID_ARG
+    # fp32 weight refused
+    st = lib.bi_pack_weight(_r(_t([64, 256], dtype=2)), FAKE, 1 << 20, ctypes.byref(desc), None)
+    assert st == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # packed descriptor with a foreign tile width
+    pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 128)
+    st = lib.bi_addmm_packed(None, _r(_t([4, 64])), ctypes.byref(pd), _r(_t([4, 256], dtype=2)), None)
+    assert st == binding.BI_ERR_INVALID_ARG
+    # K of the activations must match the packed weight
+    pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 256)
+    st = lib.bi_addmm_packed(None, _r(_t([4, 128])), ctypes.byref(pd), _r(_t([4, 256], dtype=2)), None)
+    assert st == binding.BI_ERR_SHAPE_MISMATCH

@@ -188,3 +188,67 @@ def test_linspace_batch_vs_single_row():
     assert bits_equal(out1, out2)
     ref, absum = oracle.mm(a[:1].cpu(), b.cpu())
     check_tolerance(out1, ref, absum, "linspace row 0")
+
+
+# -- packed weights ----------------------------------------------------------
+
+@pytest.mark.parametrize("layout", ["mn", "k"])
+@pytest.mark.parametrize("shape", [(1, 264, 200), (17, 256, 64), (130, 520, 1000), (257, 136, 72),
+                                   (3, 14336, 4096)])
+def test_packed_weight_is_bit_identical_to_plain(shape, layout):
+    M, N, K = shape
+    a = inputs.normal_bf16((M, K), 1.0, 80).cuda()
+    w = inputs.normal_bf16((K, N), 0.02, 81).cuda()
+    bias = inputs.normal_bf16((N,), 0.01, 82).cuda()
+    wv = w if layout == "mn" else w.t().contiguous().t()
+    packed = binding.bi_pack_weight(wv)
+    assert packed.desc.layout == (1 if layout == "mn" else 2)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        plain = binding.bi_addmm(bias, a, wv, out_dtype=out_dtype)
+        got = binding.bi_addmm_packed(bias, a, packed, out_dtype=out_dtype)
+        assert bits_equal(got, plain)
+        plain_mm = binding.bi_mm(a, wv, out_dtype=out_dtype)
+        assert bits_equal(binding.bi_addmm_packed(None, a, packed, out_dtype=out_dtype), plain_mm)
+    if M <= 300 and K <= 1000:
+        ref, absum = oracle.mm(a.cpu(), w.cpu(), bias=bias.cpu())
+        check_tolerance(binding.bi_addmm_packed(bias, a, packed, out_dtype=torch.float32), ref, absum,
+                        f"packed {shape}")
+
+
+def test_packed_weight_row0_invariant_and_validation():
+    K, N = 1024, 520
+    a = inputs.normal_bf16((300, K), 1.0, 83).cuda()
+    w = inputs.normal_bf16((K, N), 0.02, 84).cuda()
+    packed = binding.bi_pack_weight(w)
+    full = binding.bi_addmm_packed(None, a, packed)
+    for M in (1, 2, 7, 64, 129, 300):
+        assert bits_equal(binding.bi_addmm_packed(None, a[:M], packed), full[:M])
+    # a mismatched K is refused before launch
+    with pytest.raises(binding.BiError) as ei:
+        binding.bi_addmm_packed(None, a[:, :512], packed)
+    assert ei.value.status == binding.BI_ERR_SHAPE_MISMATCH
+    # a descriptor claiming a too-small buffer is refused
+    bad = binding.PackedWeight(packed.buffer, binding.BiPackedWeightDesc(
+        packed.desc.ptr, packed.desc.bytes - 16, K, N, packed.desc.layout, packed.desc.tile_n))
+    with pytest.raises(binding.BiError) as ei:
+        binding.bi_addmm_packed(None, a, bad)
+    assert ei.value.status == binding.BI_ERR_INVALID_ARG
+
+
+def test_short_a_layout_matches_general_layout_bitwise():
+    # M <= 32 runs with 32-row A stages, larger M with 128-row stages; every
+    # row must come out with the same bits either way, distractors included.
+    K, N = 2048, 776
+    a = inputs.normal_bf16((300, K), 1.0, 90).cuda()
+    w = inputs.normal_bf16((K, N), 0.02, 91).cuda()
+    bias = inputs.normal_bf16((N,), 0.01, 92).cuda()
+    general = binding.bi_addmm(bias, a, w, out_dtype=torch.float32)       # M = 300
+    packed = binding.bi_pack_weight(w)
+    for M in (1, 2, 17, 31, 32, 33):
+        assert bits_equal(binding.bi_addmm(bias, a[:M], w, out_dtype=torch.float32), general[:M]), M
+        assert bits_equal(binding.bi_addmm_packed(bias, a[:M], packed, out_dtype=torch.float32),
+                          general[:M]), M
+    for fill in (float("nan"), float("inf"), 2.0 ** 100):
+        d = a[:32].clone()
+        d[1:] = fill
+        assert bits_equal(binding.bi_addmm(bias, d, w, out_dtype=torch.float32)[:1], general[:1])
