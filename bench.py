@@ -290,18 +290,35 @@ def bits_equal(x, y) -> bool:
                                                   y.contiguous().view(torch.uint8)))
 
 
-def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
-    """The other workloads, once each: ours vs cuBLAS / cuDNN, with row-0 flags."""
+def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -> dict:
+    """The other workloads, once each: ours vs cuBLAS / cuDNN, with row-0 flags.
+    `only` restricts it to one workload (square, conv, attention, tiny)."""
     import torch.nn.functional as F
     from invariant_gemm_bi_gb300 import binding, inputs
     out = {}
+    want = (lambda name: only is None or only == name)
 
+    # large square mm, fp32 out; plain weight and packed weight
+    if want("square"):
+        _square(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
+    if want("conv"):
+        _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point_fn(peaks))
+    if want("attention"):
+        _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
+    if want("tiny"):
+        _tiny(out, binding, inputs, flush_buf, stream, reps)
+    return out
+
+
+def point_fn(peaks):
     def point(flops, nbytes, t):
         frac, bound = roofline_frac(flops, nbytes, t, peaks)
         return {"us": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
                 "gbs": round(nbytes / t / 1e9, 1), "roofline_frac": round(frac, 3), "bound": bound}
+    return point
 
-    # large square mm, fp32 out; plain weight and packed weight
+
+def _square(out, binding, inputs, flush_buf, stream, peaks, reps, point):
     a, w = inputs.square_mm(max(inputs.SQUARE_MM_M), device="cuda")
     wp = binding.bi_pack_weight(w)
     rows0 = {}
@@ -330,7 +347,8 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
                                                            for M in inputs.SQUARE_MM_M)}
     del a, w, wp
 
-    # patch-embedding conv
+
+def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
     x, wc, bc = inputs.patch_embed(max(inputs.PATCH_EMBED_B), device="cuda")
     res, y0, yc0 = [], {}, {}
     for B in inputs.PATCH_EMBED_B:
@@ -350,7 +368,9 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
                                "cudnn_sample0_bit_equal_all_B": all(bits_equal(yc0[B], yc0[1]) for B in yc0)}
     del x, wc, bc
 
-    # attention: S = QK^T/16 (fp32), P = softmax(S) (bf16), O = PV (fp32)
+
+def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
+    # S = QK^T/16 (fp32), P = softmax(S) (bf16), O = PV (fp32)
     q, k, v = inputs.attention(max(inputs.ATTENTION_B), device="cuda")
     res, o0 = [], {}
     for B in inputs.ATTENTION_B:
@@ -377,7 +397,9 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
     out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0)}
     del q, k, v
 
-    # tiny mm: launch-latency bound, report microseconds
+
+def _tiny(out, binding, inputs, flush_buf, stream, reps):
+    # launch-latency bound: report microseconds
     a, w = inputs.tiny_mm(64, device="cuda")
     res = []
     for M in inputs.TINY_MM_M:
@@ -386,7 +408,20 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int) -> dict:
         t = measure(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
         res.append({"M": M, "us": round(t * 1e6, 2)})
     out["tiny_mm"] = {"points": res}
-    return out
+
+
+def run_only(args):
+    """One workload's points (ours vs the library reference), printed as JSON."""
+    from invariant_gemm_bi_gb300 import binding, build
+    build.build()
+    binding.load()
+    torch.cuda.set_device(0)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):  # untimed passes
+        extra_sweeps(flush_buf, torch.cuda.current_stream(), load_peaks(), reps=1, only=args.only)
+    res = extra_sweeps(flush_buf, torch.cuda.current_stream(), load_peaks(), reps=max(1, args.steps),
+                       only=args.only)
+    print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, "result": res}))
 
 
 def run_ours(args, rank, local, world):
@@ -585,6 +620,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
+    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny"], default=None,
+                    help="measure only this workload (no headline line; for profiling)")
     ap.add_argument("--weight", choices=["packed", "plain"], default="packed",
                     help="weight path of the timed step (the other one is measured alongside)")
     ap.add_argument("--m-list", type=str, default=None,
@@ -593,6 +630,9 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     rank, local, world = dist_init()
+    if args.only:
+        run_only(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

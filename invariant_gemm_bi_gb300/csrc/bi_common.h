@@ -77,6 +77,9 @@ struct ConvParams {
   int32_t P;                  // Ho*Wo output positions per sample
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;  // per (sample, group) tile space
   int32_t out_f32, bias_kind, vec_store, use_tma_store;
+  int32_t patch_fast;  // stride == kernel, no padding, unit dilation: row-wise patch loader
+  int32_t x_vec16;     // image rows 16-byte aligned (16-byte loads in the patch loader)
+  int32_t w_vec8;      // weight rows 8-byte aligned (8-byte loads for A)
   unsigned int* status_word;
   uint64_t wait_limit_ns;
 };

@@ -44,6 +44,241 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+// Byte offset of bf16 element (row, c) in a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_elem(int row, int c) {
+  return (uint32_t)(row * 128 + ((((c >> 3) ^ (row & 7)) << 4) | ((c & 7) << 1)));
+}
+
+// A operand (weights of group g, rows = output channels, K contiguous):
+// general gather, 8 elements per 16-byte chunk.
+__device__ __forceinline__ void fill_a_general(const ConvParams& p, uint32_t a_dst, const uint16_t* wrow0,
+                                               int mb, int kb, int tid) {
+#pragma unroll 1
+  for (int q = tid; q < kBM * 8; q += kConvProducerThreads) {
+    const int row = q >> 3, ch = q & 7;
+    const int m = mb * kBM + row;
+    const int k0 = kb * kBK + ch * 8;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (m < p.Cog) {
+      const uint16_t* src = wrow0 + (int64_t)m * p.Kg;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = k0 + e;
+        const uint32_t h = (k < p.Kg) ? (uint32_t)__ldg(src + k) : 0u;
+        v[e >> 1] |= h << ((e & 1) * 16);
+      }
+    }
+    st_shared_v4(a_dst + sw128_offset(row, ch), v[0], v[1], v[2], v[3]);
+  }
+}
+
+// Same result when rows are 8-byte aligned (Kg % 4 == 0): one 8-byte load per
+// 4 elements, 16 consecutive threads per weight row; all 16 loads of a thread
+// are issued before any store so their latencies overlap.
+__device__ __forceinline__ void fill_a_vec8(const ConvParams& p, uint32_t a_dst, const uint16_t* wrow0,
+                                            int mb, int kb, int tid) {
+  constexpr int kPer = kBM * 16 / kConvProducerThreads;
+  uint2 v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int q = tid + i * kConvProducerThreads;
+    const int row = q >> 4, pc = q & 15;
+    const int m = mb * kBM + row;
+    const int k0 = kb * kBK + pc * 4;
+    v[i] = make_uint2(0u, 0u);
+    if (m < p.Cog) {
+      const uint16_t* src = wrow0 + (int64_t)m * p.Kg + k0;
+      if (k0 + 4 <= p.Kg) {
+        v[i] = __ldg(reinterpret_cast<const uint2*>(src));
+      } else {
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = (k0 + e < p.Kg) ? (uint32_t)__ldg(src + e) : 0u;
+        v[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int q = tid + i * kConvProducerThreads;
+    const int row = q >> 4, pc = q & 15;
+    st_shared_v2(a_dst + (uint32_t)(row * 128 + ((((pc >> 1) ^ (row & 7)) << 4) | ((pc & 1) << 3))),
+                 v[i].x, v[i].y);
+  }
+}
+
+// B operand (patches of sample b, rows = output positions, K contiguous):
+// general gather for any stride / padding / dilation.
+__device__ __forceinline__ void fill_b_general(const ConvParams& p, uint32_t b_dst, const uint16_t* ximg,
+                                               int nb, int kb, int tid) {
+  const int KHW = p.KH * p.KW;
+#pragma unroll 1
+  for (int q = tid; q < kBN * 8; q += kConvProducerThreads) {
+    const int row = q >> 3, ch = q & 7;
+    const int pos = nb * kBN + row;
+    const int k0 = kb * kBK + ch * 8;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (pos < p.P) {
+      const int oh = pos / p.Wo;
+      const int ow = pos - oh * p.Wo;
+      const int ih0 = oh * p.sh - p.ph;
+      const int iw0 = ow * p.sw - p.pw;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = k0 + e;
+        uint32_t h = 0u;
+        if (k < p.Kg) {
+          const int ci = k / KHW;
+          const int rr = k - ci * KHW;
+          const int kh = rr / p.KW;
+          const int kw = rr - kh * p.KW;
+          const int ih = ih0 + kh * p.dh;
+          const int iw = iw0 + kw * p.dw;
+          if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+            h = (uint32_t)__ldg(ximg + ((int64_t)ci * p.H + ih) * p.W + iw);
+        }
+        v[e >> 1] |= h << ((e & 1) * 16);
+      }
+    }
+    st_shared_v4(b_dst + sw128_offset(row, ch), v[0], v[1], v[2], v[3]);
+  }
+}
+
+// B operand for non-overlapping patches (stride = kernel size, no padding,
+// unit dilation): each image row (ci, ih) holds, side by side, the kw runs of
+// every patch of one output row oh.  A warp reads whole image rows with
+// coalesced (16-byte when aligned) loads and scatters each element to its
+// (patch, k) place in the swizzled tile: the same bytes fill_b_general writes.
+__device__ __forceinline__ void fill_b_patch(const ConvParams& p, uint32_t b_dst, const uint16_t* ximg,
+                                             int nb, int kb, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int k_lo = kb * kBK, k_hi = min(k_lo + kBK, p.Kg);
+  const int p_lo = nb * kBN, p_hi = min(p_lo + kBN, p.P);
+  const int ck_lo = k_lo / p.KW, ck_hi = (k_hi - 1) / p.KW;  // kernel rows (ci*KH + kh)
+  const int oh_lo = p_lo / p.Wo, oh_hi = (p_hi - 1) / p.Wo;
+  const int n_oh = oh_hi - oh_lo + 1;
+  const int items = (ck_hi - ck_lo + 1) * n_oh;
+  const int width = p.Wo * p.KW;  // image columns that belong to a patch
+  // Zero what no image element lands on: k >= Kg columns, rows past P.
+  const int valid_rows = p_hi - p_lo, valid_cols = k_hi - k_lo;
+  if (valid_rows < kBN || valid_cols < kBK) {
+    for (int q = tid; q < kBN * 8; q += kConvProducerThreads) {
+      const int row = q >> 3, ch = q & 7;
+      if (row >= valid_rows || ch * 8 >= valid_cols) {
+        st_shared_v4(b_dst + sw128_offset(row, ch), 0u, 0u, 0u, 0u);
+      } else if (ch * 8 + 8 > valid_cols) {
+        for (int c = valid_cols; c < ch * 8 + 8; ++c) st_shared_u16(b_dst + sw128_elem(row, c), 0);
+      }
+    }
+  }
+  // Rows are taken kBatch at a time per warp: all loads of a batch are issued
+  // before any element is scattered, so their latencies overlap.
+  constexpr int kBatch = 8;
+  constexpr int kWarps = kConvProducerThreads / 32;
+  if (p.x_vec16 && (p.KW & 1) == 0 && width <= 256) {
+    // Pair path: a lane's 8 elements are 4 (kw, kw+1) pairs at fixed patch
+    // columns for every image row (KW even: a pair never straddles a patch and
+    // starts at an even k, so it is one aligned 32-bit shared-memory word).
+    const int e0 = lane * 8;
+    int ow_i[4], kw_i[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + 2 * i;
+      ow_i[i] = e / p.KW;
+      kw_i[i] = e - ow_i[i] * p.KW;
+    }
+    if (e0 >= width) return;
+    for (int base = warp; base < items; base += kWarps * kBatch) {
+      uint4 raw[kBatch];
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int it = base + r * kWarps;
+        raw[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (it < items) {
+          const int ck = ck_lo + it / n_oh;
+          const int oh = oh_lo + it - (it / n_oh) * n_oh;
+          const int ci = ck / p.KH, kh = ck - ci * p.KH;
+          raw[r] = __ldg(reinterpret_cast<const uint4*>(
+              ximg + ((int64_t)ci * p.H + (int64_t)oh * p.KH + kh) * p.W + e0));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int it = base + r * kWarps;
+        if (it >= items) break;
+        const int ck = ck_lo + it / n_oh;
+        const int oh = oh_lo + it - (it / n_oh) * n_oh;
+        const int c0 = ck * p.KW - k_lo;      // column of kw = 0 in this k block
+        const int row0 = oh * p.Wo - p_lo;    // tile row of ow = 0
+        const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + kw_i[i];
+          const int row = row0 + ow_i[i];
+          // ow_i < Wo: columns past the last whole patch belong to no patch
+          if (ow_i[i] < p.Wo && c >= 0 && c < valid_cols && row >= 0 && row < valid_rows)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(b_dst + sw128_elem(row, c)), "r"(w4[i])
+                         : "memory");
+        }
+      }
+    }
+    return;
+  }
+  for (int base = warp; base < items; base += kWarps * kBatch) {
+    for (int e0 = lane * 8; e0 < width; e0 += 256) {
+      uint4 raw[kBatch];
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int it = base + r * kWarps;
+        raw[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (it < items) {
+          const int ck = ck_lo + it / n_oh;
+          const int oh = oh_lo + it - (it / n_oh) * n_oh;
+          const int ci = ck / p.KH, kh = ck - ci * p.KH;
+          const uint16_t* row_ptr = ximg + ((int64_t)ci * p.H + (int64_t)oh * p.KH + kh) * p.W;
+          if (p.x_vec16) {
+            raw[r] = __ldg(reinterpret_cast<const uint4*>(row_ptr + e0));
+          } else {
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = (e0 + j < width) ? (uint32_t)__ldg(row_ptr + e0 + j) : 0u;
+            raw[r] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                h[6] | (h[7] << 16));
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int it = base + r * kWarps;
+        if (it >= items) break;
+        const int ck = ck_lo + it / n_oh;
+        const int oh = oh_lo + it - (it / n_oh) * n_oh;
+        const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+        int ow = e0 / p.KW;
+        int kw = e0 - ow * p.KW;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = ck * p.KW + kw;
+          const int pp = oh * p.Wo + ow;
+          if (e0 + j < width && k >= k_lo && k < k_hi && pp >= p_lo && pp < p_hi)
+            st_shared_u16(b_dst + sw128_elem(pp - p_lo, k - k_lo),
+                          (uint16_t)(w4[j >> 1] >> ((j & 1) * 16)));
+          if (++kw == p.KW) {
+            kw = 0;
+            ++ow;
+          }
+        }
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_constant__ ConvParams p) {
   using Lay = ConvLayout;
   extern __shared__ uint8_t smem_raw[];
@@ -91,7 +326,6 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
   if (warp < 4) {
     // ---- producers: gather W rows and patch elements for each K block ----
     const int tid = threadIdx.x;
-    const int KHW = p.KH * p.KW;
     const uint16_t* __restrict__ xg = p.x;
     const uint16_t* __restrict__ wg = p.w;
     uint32_t it = 0;
@@ -112,55 +346,14 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
         }
         const uint32_t a_dst = sA + s * Lay::A_BYTES;
         const uint32_t b_dst = sB + s * Lay::B_BYTES;
-        // A: 128 rows (output channels of the group) x 8 chunks of 8 k.
-#pragma unroll 1
-        for (int q = tid; q < kBM * 8; q += kConvProducerThreads) {
-          const int row = q >> 3, ch = q & 7;
-          const int m = tc.mb * kBM + row;
-          const int k0 = kb * kBK + ch * 8;
-          uint32_t v[4] = {0u, 0u, 0u, 0u};
-          if (m < p.Cog) {
-            const uint16_t* src = wrow0 + (int64_t)m * p.Kg;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int k = k0 + e;
-              const uint32_t h = (k < p.Kg) ? (uint32_t)__ldg(src + k) : 0u;
-              v[e >> 1] |= h << ((e & 1) * 16);
-            }
-          }
-          st_shared_v4(a_dst + sw128_offset(row, ch), v[0], v[1], v[2], v[3]);
-        }
-        // B: kBN rows (output positions) x 8 chunks of 8 k.
-#pragma unroll 1
-        for (int q = tid; q < kBN * 8; q += kConvProducerThreads) {
-          const int row = q >> 3, ch = q & 7;
-          const int pos = tc.nb * kBN + row;
-          const int k0 = kb * kBK + ch * 8;
-          uint32_t v[4] = {0u, 0u, 0u, 0u};
-          if (pos < p.P) {
-            const int oh = pos / p.Wo;
-            const int ow = pos - oh * p.Wo;
-            const int ih0 = oh * p.sh - p.ph;
-            const int iw0 = ow * p.sw - p.pw;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int k = k0 + e;
-              uint32_t h = 0u;
-              if (k < p.Kg) {
-                const int ci = k / KHW;
-                const int rr = k - ci * KHW;
-                const int kh = rr / p.KW;
-                const int kw = rr - kh * p.KW;
-                const int ih = ih0 + kh * p.dh;
-                const int iw = iw0 + kw * p.dw;
-                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
-                  h = (uint32_t)__ldg(ximg + ((int64_t)ci * p.H + ih) * p.W + iw);
-              }
-              v[e >> 1] |= h << ((e & 1) * 16);
-            }
-          }
-          st_shared_v4(b_dst + sw128_offset(row, ch), v[0], v[1], v[2], v[3]);
-        }
+        if (p.w_vec8)
+          fill_a_vec8(p, a_dst, wrow0, tc.mb, kb, tid);
+        else
+          fill_a_general(p, a_dst, wrow0, tc.mb, kb, tid);
+        if (p.patch_fast)
+          fill_b_patch(p, b_dst, ximg, tc.nb, kb, tid);
+        else
+          fill_b_general(p, b_dst, ximg, tc.nb, kb, tid);
         fence_proxy_async_smem();
         mbar_arrive(bars.full(s));
         ++it;
@@ -243,6 +436,12 @@ bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* w
   p.bias_kind = cp.bias_kind;
   const int esz = cp.out_f32 ? 4 : 2;
   p.vec_store = ((reinterpret_cast<uintptr_t>(cp.y) % 16) == 0 && ((int64_t)p.P * esz) % 16 == 0) ? 1 : 0;
+  p.patch_fast = (cp.sh == cp.KH && cp.sw == cp.KW && cp.ph == 0 && cp.pw == 0 && cp.dh == 1 &&
+                  cp.dw == 1)
+                     ? 1
+                     : 0;
+  p.x_vec16 = ((reinterpret_cast<uintptr_t>(cp.x) % 16) == 0 && cp.W % 8 == 0) ? 1 : 0;
+  p.w_vec8 = ((reinterpret_cast<uintptr_t>(cp.w) % 8) == 0 && p.Kg % 4 == 0) ? 1 : 0;
   p.use_tma_store = encode_output_map(&p.tma_y, cp.y, cp.out_f32 != 0, cp.B * cp.groups, p.Cog, p.P,
                                       p.P, (int64_t)p.Cog * p.P)
                         ? 1

@@ -4,10 +4,11 @@
 // Softmax: one warp owns one row ("ai-infra handbook: deterministic
 // inference", section on normalisation and softmax: each row is reduced by
 // one block in a fixed order, never split across blocks because there are few
-// rows).  Lane t takes elements t, t+32, t+64, ... in ascending order; the 32
-// lane partials are combined by a fixed xor-butterfly, which gives every lane
-// the same bits (fp32 addition is commutative).  The order depends only on the
-// element index, never on the number of rows.
+// rows).  The row is cut into groups of 4 consecutive elements; lane t owns
+// groups t, t+32, t+64, ... and sums its elements in ascending index order;
+// the 32 lane partials are combined by a fixed xor-butterfly, which gives
+// every lane the same bits (fp32 addition is commutative).  The order depends
+// only on the element index, never on the number of rows or on alignment.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -19,7 +20,7 @@
 namespace bi {
 
 constexpr int kSoftmaxWarps = 8;
-constexpr int kSoftmaxRegCols = 32;  // rows up to 32*32 = 1024 columns stay in registers
+constexpr int kSoftmaxRegGroups = 8;  // rows up to 32*8*4 = 1024 columns stay in registers
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -33,60 +34,115 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void store_prob(const SoftmaxParams& p, int64_t row, int64_t j, float v) {
-  if (p.out_f32)
-    reinterpret_cast<float*>(p.p)[row * p.ld_p + j] = v;
-  else
-    reinterpret_cast<__nv_bfloat16*>(p.p)[row * p.ld_p + j] = __float2bfloat16_rn(v);
+// Group g of a row: elements 4g .. 4g+3 (those below N); absent ones read -inf.
+template <bool VEC>
+__device__ __forceinline__ float4 load_group(const float* s, int64_t g, int64_t N) {
+  const int64_t j = 4 * g;
+  if (VEC && j + 4 <= N) return __ldg(reinterpret_cast<const float4*>(s + j));
+  float4 v;
+  v.x = j + 0 < N ? __ldg(s + j + 0) : -INFINITY;
+  v.y = j + 1 < N ? __ldg(s + j + 1) : -INFINITY;
+  v.z = j + 2 < N ? __ldg(s + j + 2) : -INFINITY;
+  v.w = j + 3 < N ? __ldg(s + j + 3) : -INFINITY;
+  return v;
 }
 
-// N <= 32 * kSoftmaxRegCols: the row is read once and kept in registers.
+template <bool VEC>
+__device__ __forceinline__ void store_group(const SoftmaxParams& p, int64_t row, int64_t g, float4 v) {
+  const int64_t j = 4 * g;
+  if (p.out_f32) {
+    float* dst = reinterpret_cast<float*>(p.p) + row * p.ld_p + j;
+    if (VEC && j + 4 <= p.N) {
+      *reinterpret_cast<float4*>(dst) = v;
+    } else {
+      const float f[4] = {v.x, v.y, v.z, v.w};
+      for (int i = 0; i < 4 && j + i < p.N; ++i) dst[i] = f[i];
+    }
+  } else {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.p) + row * p.ld_p + j;
+    if (VEC && j + 4 <= p.N) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    } else {
+      const float f[4] = {v.x, v.y, v.z, v.w};
+      for (int i = 0; i < 4 && j + i < p.N; ++i) dst[i] = __float2bfloat16_rn(f[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ float group_max(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+
+// e = exp(v - mx) for the present elements (absent -inf -> 0 and not added);
+// partial sum += e in ascending element order.
+__device__ __forceinline__ float4 group_exp_sum(float4 v, float mx, int64_t j, int64_t N, float& sum) {
+  float4 e;
+  e.x = j + 0 < N ? expf(__fsub_rn(v.x, mx)) : 0.0f;
+  e.y = j + 1 < N ? expf(__fsub_rn(v.y, mx)) : 0.0f;
+  e.z = j + 2 < N ? expf(__fsub_rn(v.z, mx)) : 0.0f;
+  e.w = j + 3 < N ? expf(__fsub_rn(v.w, mx)) : 0.0f;
+  if (j + 0 < N) sum = __fadd_rn(sum, e.x);
+  if (j + 1 < N) sum = __fadd_rn(sum, e.y);
+  if (j + 2 < N) sum = __fadd_rn(sum, e.z);
+  if (j + 3 < N) sum = __fadd_rn(sum, e.w);
+  return e;
+}
+
+__device__ __forceinline__ float4 group_div(float4 e, float sum) {
+  return make_float4(__fdiv_rn(e.x, sum), __fdiv_rn(e.y, sum), __fdiv_rn(e.z, sum), __fdiv_rn(e.w, sum));
+}
+
+// N <= 32 * 4 * kSoftmaxRegGroups: the row is read once and kept in registers.
+template <bool VEC>
 __global__ void __launch_bounds__(kSoftmaxWarps * 32) softmax_reg_kernel(const SoftmaxParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kSoftmaxWarps + (threadIdx.x >> 5);
   if (row >= p.R) return;
   const float* s = p.s + row * p.ld_s;
-  const int N = (int)p.N;
-  float v[kSoftmaxRegCols];
+  const int64_t groups = (p.N + 3) / 4;
+  float4 v[kSoftmaxRegGroups];
   float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < kSoftmaxRegCols; ++i) {
-    const int j = lane + 32 * i;
-    v[i] = j < N ? __ldg(s + j) : -INFINITY;
-    mx = fmaxf(mx, v[i]);
+  for (int i = 0; i < kSoftmaxRegGroups; ++i) {
+    const int64_t g = lane + 32 * i;
+    v[i] = g < groups ? load_group<VEC>(s, g, p.N) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   }
+#pragma unroll
+  for (int i = 0; i < kSoftmaxRegGroups; ++i) mx = fmaxf(mx, group_max(v[i]));
   mx = warp_max(mx);
   float sum = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kSoftmaxRegCols; ++i) {
-    const int j = lane + 32 * i;
-    if (j < N) {
-      v[i] = expf(__fsub_rn(v[i], mx));
-      sum = __fadd_rn(sum, v[i]);
-    }
+  for (int i = 0; i < kSoftmaxRegGroups; ++i) {
+    const int64_t g = lane + 32 * i;
+    if (g < groups) v[i] = group_exp_sum(v[i], mx, 4 * g, p.N, sum);
   }
   sum = warp_sum(sum);
 #pragma unroll
-  for (int i = 0; i < kSoftmaxRegCols; ++i) {
-    const int j = lane + 32 * i;
-    if (j < N) store_prob(p, row, j, __fdiv_rn(v[i], sum));
+  for (int i = 0; i < kSoftmaxRegGroups; ++i) {
+    const int64_t g = lane + 32 * i;
+    if (g < groups) store_group<VEC>(p, row, g, group_div(v[i], sum));
   }
 }
 
 // Any N: the same arithmetic in the same order, re-reading the row.
+template <bool VEC>
 __global__ void __launch_bounds__(kSoftmaxWarps * 32) softmax_loop_kernel(const SoftmaxParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kSoftmaxWarps + (threadIdx.x >> 5);
   if (row >= p.R) return;
   const float* s = p.s + row * p.ld_s;
+  const int64_t groups = (p.N + 3) / 4;
   float mx = -INFINITY;
-  for (int64_t j = lane; j < p.N; j += 32) mx = fmaxf(mx, __ldg(s + j));
+  for (int64_t g = lane; g < groups; g += 32) mx = fmaxf(mx, group_max(load_group<VEC>(s, g, p.N)));
   mx = warp_max(mx);
   float sum = 0.0f;
-  for (int64_t j = lane; j < p.N; j += 32) sum = __fadd_rn(sum, expf(__fsub_rn(__ldg(s + j), mx)));
+  for (int64_t g = lane; g < groups; g += 32) group_exp_sum(load_group<VEC>(s, g, p.N), mx, 4 * g, p.N, sum);
   sum = warp_sum(sum);
-  for (int64_t j = lane; j < p.N; j += 32)
-    store_prob(p, row, j, __fdiv_rn(expf(__fsub_rn(__ldg(s + j), mx)), sum));
+  for (int64_t g = lane; g < groups; g += 32) {
+    float dummy = 0.0f;
+    const float4 e = group_exp_sum(load_group<VEC>(s, g, p.N), mx, 4 * g, p.N, dummy);
+    store_group<VEC>(p, row, g, group_div(e, sum));
+  }
 }
 
 bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::string* why) {
@@ -95,10 +151,22 @@ bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::stri
     *why = "too many rows";
     return BI_ERR_INVALID_ARG;
   }
-  if (sp.N <= 32 * kSoftmaxRegCols)
-    softmax_reg_kernel<<<(unsigned)blocks, kSoftmaxWarps * 32, 0, stream>>>(sp);
-  else
-    softmax_loop_kernel<<<(unsigned)blocks, kSoftmaxWarps * 32, 0, stream>>>(sp);
+  // 16-byte loads / 8- or 16-byte stores when every row start is aligned.
+  const int esz = sp.out_f32 ? 4 : 2;
+  const bool vec = reinterpret_cast<uintptr_t>(sp.s) % 16 == 0 && (sp.ld_s * 4) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(sp.p) % (4 * esz) == 0 && (sp.ld_p * esz) % (4 * esz) == 0;
+  const dim3 grid((unsigned)blocks), block(kSoftmaxWarps * 32);
+  if (sp.N <= 32 * 4 * kSoftmaxRegGroups) {
+    if (vec)
+      softmax_reg_kernel<true><<<grid, block, 0, stream>>>(sp);
+    else
+      softmax_reg_kernel<false><<<grid, block, 0, stream>>>(sp);
+  } else {
+    if (vec)
+      softmax_loop_kernel<true><<<grid, block, 0, stream>>>(sp);
+    else
+      softmax_loop_kernel<false><<<grid, block, 0, stream>>>(sp);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("softmax launch: ") + cudaGetErrorString(e);

@@ -115,6 +115,14 @@ CONV_CASES = [
     (3, 6, 17, 15, 9, 2, 3, 2, 2, 1, 3, torch.float32),
     (2, 3, 28, 28, 200, 14, 14, 14, 0, 1, 1, torch.bfloat16),
     (1, 16, 40, 40, 130, 3, 3, 1, 1, 1, 1, torch.float32),
+    # non-overlapping patches (the row-wise patch loader): grouped, partial tile,
+    # rows not 16-byte aligned, K not a multiple of 4
+    (2, 4, 30, 45, 6, 5, 3, (5, 3), 0, 1, 2, torch.float32),
+    (3, 3, 64, 48, 130, 8, 8, 8, 0, 1, 1, torch.bfloat16),
+    (2, 3, 70, 70, 40, 7, 7, 7, 0, 1, 1, torch.float32),
+    # pair path with image columns past the last patch (W = 48, Wo*KW = 42)
+    (2, 2, 20, 48, 24, 4, 6, (4, 6), 0, 1, 1, torch.float32),
+    (1, 3, 32, 40, 16, 4, 4, 4, 0, 1, 1, torch.bfloat16),
 ]
 
 
@@ -153,3 +161,15 @@ def test_bmm_bf16_output_and_batch_strides():
     check_tolerance(c, ref, absum, "bmm bf16")
     c1 = binding.bi_bmm(a[2:3].cuda(), b[2:3].cuda(), alpha=0.5, out_dtype=torch.bfloat16)
     assert bits_equal(c1, c[2:3])
+
+
+def test_softmax_alignment_does_not_change_bits():
+    # 16-byte rows take the vector path, shifted rows the scalar one: same order, same bits
+    s = inputs.normal_bf16((64, 816), 2.0, 61).float().cuda()
+    store = torch.zeros(64, 820, device="cuda")
+    shifted = store[:, 1:817]
+    shifted.copy_(s)
+    for od in (torch.bfloat16, torch.float32):
+        a = binding.bi_softmax_lastdim(s, out_dtype=od)
+        b = binding.bi_softmax_lastdim(shifted, out_dtype=od)
+        assert bits_equal(a, b)
