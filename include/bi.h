@@ -129,8 +129,9 @@ bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tenso
 
 /*
  * p[r,:] = softmax(s[r,:]) over the last dimension, per row r:
- *   mx = max_j s[r,j];  e_j = expf(s[r,j] - mx);  p[r,j] = e_j / sum_j e_j,
- *   sums in fp32 in a fixed order set by the element index only.
+ *   mx = max_j s[r,j];  e_j = expf(s[r,j] - mx);  p[r,j] = e_j * RN(1 / sum_j e_j),
+ *   sums in fp32 in a fixed order set by the element index only (4-element
+ *   groups g, lane g mod 32 of one warp, then a fixed butterfly).
  *   s: [R,N] fp32, unit stride on N;  p: [R,N] bf16 or fp32, unit stride on N.
  */
 bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream);

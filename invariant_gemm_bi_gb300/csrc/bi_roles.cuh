@@ -142,20 +142,45 @@ __device__ __forceinline__ float load_bias(const OutDesc& o, int64_t idx) {
   return reinterpret_cast<const float*>(o.bias)[idx * o.bias_stride];
 }
 
+// Bias values a warp needs for one tile, loaded before the accumulator is
+// ready so their latency hides behind the tile's main loop: per row, this
+// thread's row; per column, lane t holds the bias of column t of each
+// 32-column chunk j (broadcast to the warp with shuffles when used).
+struct TileBias {
+  float row;
+  float col[kBN / 32];
+};
+
+__device__ __forceinline__ void load_tile_bias(const OutDesc& o, int l, int m, int n_base, int lane,
+                                               TileBias& tb) {
+  if (!o.bias_kind) return;
+  if (o.bias_per_row) {
+    tb.row = (m < o.M) ? load_bias(o, (int64_t)(l % o.bias_groups) * o.M + m) : 0.0f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kBN / 32; ++j) {
+      const int n = n_base + j * 32 + lane;
+      tb.col[j] = (n < o.N) ? load_bias(o, n) : 0.0f;
+    }
+  }
+}
+
 // f = acc * alpha (+ bias), each a separately rounded fp32 operation.
-__device__ __forceinline__ void epilogue_math(const OutDesc& o, int l, int m, int n0,
+__device__ __forceinline__ void epilogue_math(const OutDesc& o, int j, const TileBias& tb,
                                               const uint32_t (&v)[32], float (&f)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), o.alpha);
   if (o.bias_kind) {
     if (o.bias_per_row) {
-      const float bv = (m < o.M) ? load_bias(o, (int64_t)(l % o.bias_groups) * o.M + m) : 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) f[i] = __fadd_rn(f[i], bv);
+      for (int i = 0; i < 32; ++i) f[i] = __fadd_rn(f[i], tb.row);
     } else {
+      float bj = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (n0 + i < o.N) f[i] = __fadd_rn(f[i], load_bias(o, n0 + i));
+      for (int jj = 0; jj < kBN / 32; ++jj)
+        if (jj == j) bj = tb.col[jj];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] = __fadd_rn(f[i], __shfl_sync(0xffffffffu, bj, i));
     }
   }
 }
@@ -230,12 +255,14 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
   for (int tile = blockIdx.x; tile < num_tiles; tile += stride, ++local) {
     const uint32_t buf = local & 1;
     const uint32_t use = local >> 1;
+    const TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
+    const int m0 = tc.mb * kBM + q * 32;
+    TileBias tb;
+    load_tile_bias(o, tc.l, m0 + lane, tc.nb * kBN, lane, tb);
     const bool ok = mbar_wait_bounded(bars.tfull(buf), use & 1, w.abort, w.status_word,
                                       w.limit_ns, status_code(6, kSiteEpilogueTmemFull));
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after_sync();
-    const TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
-    const int m0 = tc.mb * kBM + q * 32;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kBN;
 #pragma unroll 1
     for (int j = 0; j < kBN / 32; ++j) {
@@ -244,7 +271,7 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
       tmem_load_wait();
       const int n0 = tc.nb * kBN + j * 32;
       float f[32];
-      epilogue_math(o, tc.l, m0 + lane, n0, v, f);
+      epilogue_math(o, j, tb, v, f);
       if (o.tma_c) {
         if (n0 < o.N && m0 < o.M) {  // boxes wholly past the matrix are skipped, not issued
           const uint32_t sbuf = stage_base + (chunk & 1) * kStageOutBytes;

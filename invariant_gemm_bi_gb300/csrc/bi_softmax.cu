@@ -77,6 +77,14 @@ __device__ __forceinline__ float group_max(float4 v) { return fmaxf(fmaxf(v.x, v
 // partial sum += e in ascending element order.
 __device__ __forceinline__ float4 group_exp_sum(float4 v, float mx, int64_t j, int64_t N, float& sum) {
   float4 e;
+  if (j + 4 <= N) {  // whole group: same operations without the bounds tests
+    e.x = expf(__fsub_rn(v.x, mx));
+    e.y = expf(__fsub_rn(v.y, mx));
+    e.z = expf(__fsub_rn(v.z, mx));
+    e.w = expf(__fsub_rn(v.w, mx));
+    sum = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(sum, e.x), e.y), e.z), e.w);
+    return e;
+  }
   e.x = j + 0 < N ? expf(__fsub_rn(v.x, mx)) : 0.0f;
   e.y = j + 1 < N ? expf(__fsub_rn(v.y, mx)) : 0.0f;
   e.z = j + 2 < N ? expf(__fsub_rn(v.z, mx)) : 0.0f;
@@ -88,8 +96,11 @@ __device__ __forceinline__ float4 group_exp_sum(float4 v, float mx, int64_t j, i
   return e;
 }
 
-__device__ __forceinline__ float4 group_div(float4 e, float sum) {
-  return make_float4(__fdiv_rn(e.x, sum), __fdiv_rn(e.y, sum), __fdiv_rn(e.z, sum), __fdiv_rn(e.w, sum));
+// p = e * RN(1 / sum): one correctly rounded reciprocal per row, one
+// multiply per element.
+__device__ __forceinline__ float4 group_scale(float4 e, float rinv) {
+  return make_float4(__fmul_rn(e.x, rinv), __fmul_rn(e.y, rinv), __fmul_rn(e.z, rinv),
+                     __fmul_rn(e.w, rinv));
 }
 
 // N <= 32 * 4 * kSoftmaxRegGroups: the row is read once and kept in registers.
@@ -117,10 +128,11 @@ __global__ void __launch_bounds__(kSoftmaxWarps * 32) softmax_reg_kernel(const S
     if (g < groups) v[i] = group_exp_sum(v[i], mx, 4 * g, p.N, sum);
   }
   sum = warp_sum(sum);
+  const float rinv = __frcp_rn(sum);
 #pragma unroll
   for (int i = 0; i < kSoftmaxRegGroups; ++i) {
     const int64_t g = lane + 32 * i;
-    if (g < groups) store_group<VEC>(p, row, g, group_div(v[i], sum));
+    if (g < groups) store_group<VEC>(p, row, g, group_scale(v[i], rinv));
   }
 }
 
@@ -138,10 +150,11 @@ __global__ void __launch_bounds__(kSoftmaxWarps * 32) softmax_loop_kernel(const 
   float sum = 0.0f;
   for (int64_t g = lane; g < groups; g += 32) group_exp_sum(load_group<VEC>(s, g, p.N), mx, 4 * g, p.N, sum);
   sum = warp_sum(sum);
+  const float rinv = __frcp_rn(sum);
   for (int64_t g = lane; g < groups; g += 32) {
     float dummy = 0.0f;
     const float4 e = group_exp_sum(load_group<VEC>(s, g, p.N), mx, 4 * g, p.N, dummy);
-    store_group<VEC>(p, row, g, group_div(e, sum));
+    store_group<VEC>(p, row, g, group_scale(e, rinv));
   }
 }
 
