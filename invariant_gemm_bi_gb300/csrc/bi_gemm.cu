@@ -74,7 +74,6 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, ui
   const TileCoord& tc = c.tc;
   const uint32_t fb = bars.full(s);
   mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
-  tma_load_3d(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
   const uint32_t b_dst = sB + s * Lay::B_BYTES;
   if (B_PACKED) {
     const uint8_t* src = p.b_packed + (int64_t)c.kb * p.packed_kb_stride + (int64_t)tc.nb * Lay::B_BYTES;
@@ -86,6 +85,7 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, ui
   } else {
     tma_load_3d(b_dst, &p.tma_b, fb, c.kb * kBK, tc.nb * kBN, tc.l);
   }
+  tma_load_3d(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
 }
 
 __device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int stride) {

@@ -243,6 +243,32 @@ __device__ __forceinline__ void stage_32(const OutDesc& o, uint32_t sbuf, int la
   }
 }
 
+// Converts and stores chunk j (32 columns) of this warp's 32 rows.
+__device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const TileBias& tb,
+                                               const uint32_t (&v)[32], const TileCoord& tc, int m0,
+                                               int lane, uint32_t stage_base, uint32_t& chunk) {
+  const int n0 = tc.nb * kBN + j * 32;
+  float f[32];
+  epilogue_math(o, j, tb, v, f);
+  if (o.tma_c) {
+    const uint32_t sbuf = stage_base + (chunk & 1) * kStageOutBytes;
+    if (chunk >= 2) {  // the store issued two chunks ago must have read this buffer
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+    }
+    stage_32(o, sbuf, lane, f);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(o.tma_c, sbuf, n0, m0, tc.l);
+      bulk_commit();
+    }
+    ++chunk;
+  } else {
+    store_32_direct(o, tc.l, m0 + lane, n0, f);
+  }
+}
+
 // One warp of the epilogue group: drains TMEM lane quadrant q (rows
 // 32q .. 32q+31 of each tile) for every tile of this CTA.  stage_base: this
 // warp's two staging buffers (used when o.tma_c is set).
@@ -264,32 +290,23 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after_sync();
     const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kBN;
+    // Chunks holding any output: none when all 32 rows of this quadrant are
+    // past M, and none past N.
+    const int n_left = o.N - tc.nb * kBN;
+    const int n_chunks = (m0 < o.M) ? min(kBN / 32, (n_left + 31) / 32) : 0;
+    // Two register sets: the next chunk's TMEM load is in flight while the
+    // current chunk is converted and stored.
+    uint32_t va[32], vb[32];
+    if (n_chunks > 0) tmem_load_32cols(lane_addr, va);
 #pragma unroll 1
-    for (int j = 0; j < kBN / 32; ++j) {
-      uint32_t v[32];
-      tmem_load_32cols(lane_addr + j * 32, v);
-      tmem_load_wait();
-      const int n0 = tc.nb * kBN + j * 32;
-      float f[32];
-      epilogue_math(o, j, tb, v, f);
-      if (o.tma_c) {
-        if (n0 < o.N && m0 < o.M) {  // boxes wholly past the matrix are skipped, not issued
-          const uint32_t sbuf = stage_base + (chunk & 1) * kStageOutBytes;
-          if (chunk >= 2) {  // the store issued two chunks ago must have read this buffer
-            if (lane == 0) bulk_wait_read_1();
-            __syncwarp();
-          }
-          stage_32(o, sbuf, lane, f);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(o.tma_c, sbuf, n0, m0, tc.l);
-            bulk_commit();
-          }
-          ++chunk;
-        }
-      } else {
-        store_32_direct(o, tc.l, m0 + lane, n0, f);
+    for (int j = 0; j < n_chunks; j += 2) {
+      tmem_load_wait(va);
+      if (j + 1 < n_chunks) tmem_load_32cols(lane_addr + (j + 1) * 32, vb);
+      epilogue_chunk(o, j, tb, va, tc, m0, lane, stage_base, chunk);
+      if (j + 1 < n_chunks) {
+        tmem_load_wait(vb);
+        if (j + 2 < n_chunks) tmem_load_32cols(lane_addr + (j + 2) * 32, va);
+        epilogue_chunk(o, j + 1, tb, vb, tc, m0, lane, stage_base, chunk);
       }
     }
     tc_fence_before_sync();
