@@ -30,6 +30,7 @@ struct DevState {
   int num_sms = 0;
   unsigned int* status_word = nullptr;
   bool smem_set[16] = {};
+  int pairs[16] = {};  // resident 2-CTA clusters per kernel slot (0: not yet asked)
 };
 DevState g_dev[kMaxDevices];
 
@@ -148,6 +149,31 @@ cudaError_t set_smem_once(const void* func, int bytes, int slot) {
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) d.smem_set[slot] = true;
   return e;
+}
+
+cudaError_t pair_capacity(const void* func, int threads, int dyn_bytes, int slot, int* pairs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].pairs[slot] > 0) {
+      *pairs = g_dev[dev].pairs[slot];
+      return cudaSuccess;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = dyn_bytes;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) n = 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_dev[dev].pairs[slot] = n;
+  *pairs = n;
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
@@ -571,9 +597,11 @@ extern "C" bi_status bi_device_status(bi_stream stream) {
   if (e != cudaSuccess) return finish(BI_ERR_CUDA, std::string("status clear: ") + cudaGetErrorString(e));
   static const char* kSites[] = {"?", "producer waiting for a free stage", "MMA waiting for a full stage",
                                  "MMA waiting for a free accumulator", "epilogue waiting for an accumulator",
-                                 "draining in-flight work", "debug wait", "conv producer waiting for a free stage"};
+                                 "draining in-flight work", "debug wait", "conv producer waiting for a free stage",
+                                 "weight packer waiting for its tile"};
   const unsigned site = (v >> 8) & 0xFF;
-  why = std::string("device wait ran out: ") + (site < 8 ? kSites[site] : "?");
+  why = std::string("device wait ran out: ") +
+        (site < sizeof(kSites) / sizeof(kSites[0]) ? kSites[site] : "?");
   return finish((bi_status)(v & 0xFF), why);
 }
 

@@ -44,10 +44,12 @@ __host__ __device__ constexpr unsigned int status_code(unsigned int bi_err, unsi
 }
 
 struct GemmParams {
-  CUtensorMap tma_a;  // A as [L][M][K] bf16, box {64, 128, 1}, 128B swizzle
-  CUtensorMap tma_b;  // K-major B as [L][N][K], box {64, BN, 1}; MN-major as [L][K][N], box {64, 64, 1}
+  CUtensorMap tma_a;  // A as [L][M][K] bf16, box {64, 128 (32 for M <= 32), 1}, 128B swizzle
+  // B: K-major as [L][N][K], box {64, BN/2, 1}; MN-major as [L][K][N], box
+  // {64, 64, 1} (both 128B swizzle); packed as [rows][64] (128-byte rows of
+  // the packed image), box {64, BN/2*64*2/128, 1}, no swizzle
+  CUtensorMap tma_b;
   CUtensorMap tma_c;  // C as [L][M][N], box {32, 32, 1} (fp32: 128B swizzle, bf16: 64B), if use_tma_store
-  const uint8_t* b_packed;   // packed B (see kPackChunk), or null
   int64_t packed_kb_stride;  // bytes between consecutive k blocks of the packed B
   void* c;
   const void* bias;

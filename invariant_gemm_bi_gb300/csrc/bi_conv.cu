@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
     }
   } else if (warp == 4) {
     if (lane == 0)
-      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, false>(sA, sB, bars, tmem_base,
-                                                               p.num_tiles, p.k_blocks, gridDim.x, wc);
+      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, false>(
+          sA, sB, bars, tmem_base, blockIdx.x, p.num_tiles, p.k_blocks, gridDim.x, wc);
   } else {
     OutDesc o;
     o.c = p.y;
@@ -380,8 +380,8 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
     o.bias_groups = p.groups;
     o.tma_c = p.use_tma_store ? &p.tma_y : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 5) * 2 * kStageOutBytes;
-    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, gridDim.x, o,
-                  staging, wc);
+    epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,
+                  gridDim.x, o, staging, wc);
   }
 
   tc_fence_before_sync();

@@ -1,16 +1,28 @@
-// bi_gemm.cu -- persistent, warp-specialised tcgen05 GEMM for mm / addmm / bmm,
-// and the weight packer.
+// bi_gemm.cu -- persistent, warp-specialised tcgen05 GEMM for mm / addmm / bmm
+// on CTA pairs, and the weight packer.
 //
-//   warp 0      producer: A (128 x 64) and B (kBN x 64) tiles of each K block
-//               into a ring of shared-memory stages (128-byte swizzle).  A always
-//               arrives by TMA (out-of-range rows / K zero-filled by the copy
-//               engine).  B arrives either by TMA from its strided layout, or --
-//               for a packed weight -- as one contiguous 1-D bulk copy per stage
-//               of the very same shared-memory image.
-//   warp 1      TMEM allocator + single-thread UMMA issuer (fp32 accumulator in
-//               TMEM, double-buffered so the epilogue of tile i overlaps the main
-//               loop of tile i+1)
-//   warps 2..5  epilogue: tcgen05.ld -> alpha / bias -> rounding -> global
+// The kernel runs as clusters of two CTAs on the two SMs of a TPC.  A tile is
+// 256 rows x 256 columns; each CTA of the pair stages its own 128 rows of A
+// and half of the tile's columns of B, and the even CTA issues 256-row
+// tcgen05.mma (cta_group::2) instructions that read both CTAs' stages and
+// leave rows 0..127 in its own TMEM, rows 128..255 in the odd CTA's.  Every SM
+// thus ingests only half of the weight columns it multiplies -- for
+// decode-sized M, where the weight stream is the whole cost, twice as many SMs
+// stream it as with one CTA per tile.
+//
+//   warp 0      producer (each CTA): A (128 x 64) and its half of B (128 x 64)
+//               of each K block into a ring of shared-memory stages (128-byte
+//               swizzle), by TMA; the copies of both CTAs complete on the even
+//               CTA's barrier of the stage.  Out-of-range rows / K are
+//               zero-filled by the copy engine; an odd CTA whose 128 rows all
+//               lie past M loads no A (its accumulator rows are never stored).
+//               B comes from its strided layout or, for a packed weight, as
+//               128-byte rows of the image already in shared-memory order.
+//   warp 1      TMEM allocation (both CTAs, together); in the even CTA the
+//               single-thread UMMA issuer (fp32 accumulators double-buffered
+//               so the epilogue of tile i overlaps the main loop of tile i+1)
+//   warps 2..5  epilogue (each CTA, its own 128 rows): tcgen05.ld -> alpha /
+//               bias -> rounding -> global
 //
 // Batch elements of bmm are a third tile coordinate, so tiles never straddle
 // batch elements ("Batch-Invariant Kernel Design: Conv2d and Attention BMM",
@@ -26,19 +38,25 @@
 
 namespace bi {
 
-// Shared-memory plan of the GEMM.  A_ROWS = 128 is the general layout: A
-// stages hold a whole 128-row A tile, and the epilogue stages its output for
-// TMA stores.  A_ROWS = 32 is the short-A layout for problems with at most 32
-// rows (decode-sized M), where the weight stream is the whole cost: A stages
-// hold 32 rows, which frees room for more B stages in flight.  The tensor core
-// still runs the same 128 x kBN x 16 instructions in the same K order; its A
-// rows 32..127 read whatever lies beyond the 32-row stage and only produce
-// accumulator rows that are never stored (no output row reads another row's
-// A data), so every stored element is computed exactly as in the general layout.
+// Shared-memory plan of one CTA of the pair.  A_ROWS = 128 is the general
+// layout: A stages hold the CTA's whole 128-row A block, and the epilogue
+// stages its output for TMA stores.  A_ROWS = 32 is the short-A layout for
+// problems with at most 32 rows (decode-sized M), where the weight stream is
+// the whole cost: A stages hold 32 rows, which frees room for more B stages
+// in flight.  The tensor core still runs the same 256 x kGemmBN x 16 pair
+// instructions in the same K order; its A rows 32..127 read whatever lies
+// beyond the 32-row stage and only produce accumulator rows that are never
+// stored (no output row reads another row's A data), so every stored element
+// is computed exactly as in the general layout.
+// Pair tile: 256 rows x kGemmBN columns; kGemmAcc accumulators of kGemmBN
+// fp32 columns each in TMEM.
+constexpr int kGemmBN = 256;
+constexpr int kGemmAcc = 2;
+
 template <int A_ROWS>
 struct GemmLayout {
   static constexpr int A_BYTES = A_ROWS * kBK * 2;
-  static constexpr int B_BYTES = kBN * kBK * 2;
+  static constexpr int B_BYTES = (kGemmBN / 2) * kBK * 2;  // this CTA's half of the tile's columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGING_BYTES = A_ROWS == kBM ? kEpilogueStagingBytes : 0;
@@ -47,60 +65,84 @@ struct GemmLayout {
   static constexpr int A_OVERREAD = (kBM - A_ROWS) * kBK * 2;
   static constexpr int MAX_DYN = 232448;  // 227 KB, the opt-in per-block maximum
   static constexpr int FIT = (MAX_DYN - 1024 - BAR_BYTES - STAGING_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int STAGES = FIT > 16 ? 16 : FIT;
   static constexpr int DYN_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + STAGING_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2 * kBN;
+  static constexpr uint32_t TMEM_COLS = kGemmAcc * kGemmBN;
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
+  static_assert(8 * (2 * STAGES + 2 * kGemmAcc + 1) + 8 <= BAR_BYTES, "barriers fit their block");
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
   static_assert(DYN_BYTES > 116 * 1024, "one CTA per SM: TMEM is allocated whole");
-  static_assert(B_BYTES == (kBN / kPackChunk) * kPackChunkBytes, "packed stage = whole chunks");
+  static_assert(B_BYTES % kPackChunkBytes == 0, "packed half stage = whole chunks");
+  static_assert(kBN % kGemmBN == 0, "packed tiles hold whole pair tiles");
   static_assert(A_OVERREAD <= STAGES * B_BYTES, "A over-read stays inside the B stages");
 };
 
 constexpr int kGemmThreads = 192;
 
-// Producer cursor over this CTA's (tile, k block) sequence.
+// Producer cursor over this pair's (tile, k block) sequence.
 struct ProdCursor {
   int tile, kb;
   uint32_t it;
-  TileCoord tc;  // coordinates of `tile` (decoded once per tile)
+  TileCoord tc;  // coordinates of `tile` for this CTA (mb: its 128-row block)
 };
 
+__device__ __forceinline__ TileCoord pair_tile(int tile, const GemmParams& p, uint32_t crank) {
+  TileCoord tc = decode_tile(tile, p.m_tiles, p.n_tiles);
+  tc.mb = 2 * tc.mb + (int)crank;
+  return tc;
+}
+
+// One stage of this CTA: its A block (unless every one of its rows lies past
+// M) and its half of the tile's B columns, into its own shared memory.  Every
+// copy of both CTAs completes on the even CTA's full barrier of the stage,
+// which the even CTA arms with the bytes of both.
 template <bool B_MN, bool B_PACKED, int A_ROWS>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, uint32_t sB,
-                                            const PipeBars& bars, const ProdCursor& c) {
+                                            const PipeBars& bars, const ProdCursor& c,
+                                            uint32_t crank) {
   using Lay = GemmLayout<A_ROWS>;
   const uint32_t s = c.it % Lay::STAGES;
   const TileCoord& tc = c.tc;
-  const uint32_t fb = bars.full(s);
-  mbar_arrive_expect_tx(fb, Lay::STAGE_BYTES);
+  const bool a_live = tc.mb * kBM < p.M;
+  if (crank == 0) {
+    const bool peer_live = (tc.mb + 1) * kBM < p.M;
+    mbar_arrive_expect_tx(bars.full(s), 2 * Lay::B_BYTES + Lay::A_BYTES * (peer_live ? 2 : 1));
+  }
+  const uint32_t fb = cluster_map_shared(bars.full(s), 0);
   const uint32_t b_dst = sB + s * Lay::B_BYTES;
+  const int n0 = tc.nb * kGemmBN + (int)crank * (kGemmBN / 2);
   if (B_PACKED) {
-    const uint8_t* src = p.b_packed + (int64_t)c.kb * p.packed_kb_stride + (int64_t)tc.nb * Lay::B_BYTES;
-    bulk_load(b_dst, src, Lay::B_BYTES, fb);
+    // The packed weight as rows of 128 bytes: this CTA's columns n0 .. are
+    // whole 64-column chunks, B_BYTES / 128 consecutive rows of the image.
+    const int64_t byte0 = (int64_t)c.kb * p.packed_kb_stride + (int64_t)(n0 / kPackChunk) * kPackChunkBytes;
+    tma_load_3d_pair(b_dst, &p.tma_b, fb, 0, (int32_t)(byte0 / 128), 0);
   } else if (B_MN) {
 #pragma unroll
-    for (int j = 0; j < kBN / 64; ++j)
-      tma_load_3d(b_dst + j * 8192, &p.tma_b, fb, tc.nb * kBN + j * 64, c.kb * kBK, tc.l);
+    for (int j = 0; j < kGemmBN / 2 / 64; ++j)
+      tma_load_3d_pair(b_dst + j * 8192, &p.tma_b, fb, n0 + j * 64, c.kb * kBK, tc.l);
   } else {
-    tma_load_3d(b_dst, &p.tma_b, fb, c.kb * kBK, tc.nb * kBN, tc.l);
+    tma_load_3d_pair(b_dst, &p.tma_b, fb, c.kb * kBK, n0, tc.l);
   }
-  tma_load_3d(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
+  if (a_live) tma_load_3d_pair(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
 }
 
-__device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int stride) {
+__device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int stride,
+                                        uint32_t crank) {
   ++c.it;
   if (++c.kb == p.k_blocks) {
     c.kb = 0;
     c.tile += stride;
-    if (c.tile < p.num_tiles) c.tc = decode_tile(c.tile, p.m_tiles, p.n_tiles);
+    if (c.tile < p.num_tiles) c.tc = pair_tile(c.tile, p, crank);
   }
 }
 
 template <bool B_MN, bool B_PACKED, int A_ROWS>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p) {
   using Lay = GemmLayout<A_ROWS>;
-  const int stride = gridDim.x;  // grid = min(#tiles, #SMs): every CTA owns tiles
+  const uint32_t crank = cluster_ctarank();  // 0: the pair's MMA issuer
+  const int stride = gridDim.x >> 1;         // pairs; every pair owns tiles
+  const int first_tile = blockIdx.x >> 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -112,70 +154,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   bars.full0 = bar0;
   bars.empty0 = bar0 + 8 * Lay::STAGES;
   bars.tfull0 = bars.empty0 + 8 * Lay::STAGES;
-  bars.tempty0 = bars.tfull0 + 16;
-  bars.drain = bars.tempty0 + 16;
+  bars.tempty0 = bars.tfull0 + 8 * kGemmAcc;
+  bars.drain = bars.tempty0 + 8 * kGemmAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars.drain + 8 - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  ProdCursor cur{(int)blockIdx.x, 0, 0u, {0, 0, 0}};
+  ProdCursor cur{first_tile, 0, 0u, {0, 0, 0}};
 
   if (threadIdx.x == 0) {
+    // Even CTA: a stage is full when the copies of both CTAs have landed; an
+    // accumulator is free when the four epilogue warps of both CTAs have
+    // drained it.  (The odd CTA's full and tempty barriers stay unused.)
     for (int s = 0; s < Lay::STAGES; ++s) {
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kGemmAcc; ++b) {
       mbar_init(bars.tfull(b), 1);
-      mbar_init(bars.tempty(b), 4);
+      mbar_init(bars.tempty(b), 8);
     }
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    // The first ring's worth of loads needs no free-stage wait: start the
-    // memory traffic before the rest of the CTA is set up.
     tma_prefetch_desc(&p.tma_a);
-    if (!B_PACKED) tma_prefetch_desc(&p.tma_b);
-    cur.tc = decode_tile(cur.tile, p.m_tiles, p.n_tiles);
-    while (cur.it < (uint32_t)Lay::STAGES && cur.tile < p.num_tiles) {
-      issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur);
-      advance(cur, p, stride);
-    }
+    tma_prefetch_desc(&p.tma_b);
+    cur.tc = pair_tile(cur.tile, p, crank);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), Lay::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Both CTAs' barriers are initialised before any copy or signal crosses
+  // between them.  Meanwhile the even CTA starts its first ring of loads,
+  // which needs no free-stage wait and signals only its own barriers.
+  cluster_arrive_relaxed();
+  if (threadIdx.x == 0) {
+    while (crank == 0 && cur.it < (uint32_t)Lay::STAGES && cur.tile < p.num_tiles) {
+      issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur, crank);
+      advance(cur, p, stride, crank);
+    }
+  }
+  __syncwarp();
+  cluster_wait();
   const WaitCtl wc{abort_flag, p.status_word, p.wait_limit_ns};
 
   if (warp == 0) {
     if (lane == 0) {
       while (cur.tile < p.num_tiles) {
         const uint32_t s = cur.it % Lay::STAGES;
-        const uint32_t r = cur.it / Lay::STAGES;  // >= 1 here
-        if (!mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word, wc.limit_ns,
-                               status_code(6, kSiteProducerEmpty)))
+        const uint32_t r = cur.it / Lay::STAGES;
+        if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
+                                        wc.limit_ns, status_code(6, kSiteProducerEmpty)))
           break;
-        issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur);
-        advance(cur, p, stride);
+        issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur, crank);
+        advance(cur, p, stride, crank);
       }
-      // No copy may still be landing in shared memory when the CTA exits:
-      // wait (bounded) for the last fill of every stage.
+      // No copy may still be landing in shared memory, and no MMA-completion
+      // signal may still be on its way to this CTA, when it exits: wait
+      // (bounded) until the last fill of every stage has been consumed.
       const uint32_t it = cur.it;
       const uint32_t first = it > (uint32_t)Lay::STAGES ? it - Lay::STAGES : 0u;
       for (uint32_t j = first; j < it; ++j)
-        mbar_wait_bounded(bars.full(j % Lay::STAGES), (j / Lay::STAGES) & 1, nullptr,
-                          wc.status_word, wc.limit_ns, status_code(6, kSiteDrain));
+        if (!mbar_wait_bounded(bars.empty(j % Lay::STAGES), (j / Lay::STAGES) & 1, nullptr,
+                               wc.status_word, wc.limit_ns, status_code(6, kSiteDrain)))
+          break;
     }
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, B_MN>(sA, sB, bars, tmem_base, p.num_tiles,
-                                                              p.k_blocks, stride, wc);
+    if (lane == 0 && crank == 0)
+      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, B_MN, true, kGemmBN, kGemmAcc>(
+          sA, sB, bars, tmem_base, first_tile, p.num_tiles, p.k_blocks, stride, wc);
   } else {
     OutDesc o;
     o.c = p.c;
@@ -193,16 +246,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     o.bias_groups = 1;
     o.tma_c = (Lay::STAGING_BYTES > 0 && p.use_tma_store) ? &p.tma_c : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 2) * 2 * kStageOutBytes;
-    epilogue_role(warp & 3, lane, tmem_base, bars, p.num_tiles, p.m_tiles, p.n_tiles, stride, o,
-                  staging, wc);
+    epilogue_role<true, kGemmBN, kGemmAcc>(warp & 3, lane, tmem_base, bars, first_tile, p.num_tiles, p.m_tiles,
+                        p.n_tiles, stride, o, staging, wc, crank);
   }
 
+  // Neither CTA leaves while the other may still signal it or use its TMEM.
   tc_fence_before_sync();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Lay::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, Lay::TMEM_COLS);
   }
 }
 
@@ -307,24 +362,29 @@ bi_status launch_pack(const GemmProblem& g, void* dst, cudaStream_t stream, std:
   return BI_OK;
 }
 
+// Grid: two CTAs per pair, min(#tiles, #pairs that fit at once) pairs.
 template <bool B_MN, bool B_PACKED, int A_ROWS>
-static cudaError_t launch_variant(const GemmParams& p, int grid, cudaStream_t stream, int slot) {
+static cudaError_t launch_variant(const GemmParams& p, int64_t tiles, cudaStream_t stream, int slot) {
   using Lay = GemmLayout<A_ROWS>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gemm_kernel<B_MN, B_PACKED, A_ROWS>),
-                                Lay::DYN_BYTES, slot);
-  if (e == cudaSuccess)
-    gemm_kernel<B_MN, B_PACKED, A_ROWS><<<grid, kGemmThreads, Lay::DYN_BYTES, stream>>>(p);
-  return e;
+  const void* fn = reinterpret_cast<const void*>(&gemm_kernel<B_MN, B_PACKED, A_ROWS>);
+  cudaError_t e = set_smem_once(fn, Lay::DYN_BYTES, slot);
+  if (e != cudaSuccess) return e;
+  int pairs = 0;
+  e = pair_capacity(fn, kGemmThreads, Lay::DYN_BYTES, slot, &pairs);
+  if (e != cudaSuccess) return e;
+  const int grid = 2 * (int)std::min<int64_t>(tiles, pairs);
+  gemm_kernel<B_MN, B_PACKED, A_ROWS><<<grid, kGemmThreads, Lay::DYN_BYTES, stream>>>(p);
+  return cudaSuccess;
 }
 
 template <int A_ROWS>
-static cudaError_t launch_rows(const GemmProblem& g, const GemmParams& p, int grid,
+static cudaError_t launch_rows(const GemmProblem& g, const GemmParams& p, int64_t tiles,
                                cudaStream_t stream, int slot0) {
   if (g.b_packed)
-    return g.b_mn_major ? launch_variant<true, true, A_ROWS>(p, grid, stream, slot0 + 2)
-                        : launch_variant<false, true, A_ROWS>(p, grid, stream, slot0 + 3);
-  return g.b_mn_major ? launch_variant<true, false, A_ROWS>(p, grid, stream, slot0)
-                      : launch_variant<false, false, A_ROWS>(p, grid, stream, slot0 + 1);
+    return g.b_mn_major ? launch_variant<true, true, A_ROWS>(p, tiles, stream, slot0 + 2)
+                        : launch_variant<false, true, A_ROWS>(p, tiles, stream, slot0 + 3);
+  return g.b_mn_major ? launch_variant<true, false, A_ROWS>(p, tiles, stream, slot0)
+                      : launch_variant<false, false, A_ROWS>(p, tiles, stream, slot0 + 1);
 }
 
 bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* why) {
@@ -344,9 +404,17 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   if (!encode_3d(&p.tma_a, g.a, K, M, L, a_row, a_bat, kBK, short_a ? kShortARows : kBM, why))
     return BI_ERR_CUDA;
   if (g.b_packed) {
-    p.b_packed = reinterpret_cast<const uint8_t*>(g.b_packed);
+    // The packed image as [rows][64] bf16 (128-byte rows, no swizzle: the
+    // image is already in shared-memory order), boxes of 128 rows.
     p.packed_kb_stride = ((N + kBN - 1) / kBN) * (int64_t)(kBN * kBK * 2);
-  } else if (!encode_b(&p.tma_b, g, kBN, why)) {
+    const uint64_t rows = (uint64_t)((K + kBK - 1) / kBK) * (uint64_t)p.packed_kb_stride / 128;
+    const cuuint64_t dims[3] = {64, rows, 1};
+    const cuuint64_t strides[2] = {128, rows * 128};
+    const cuuint32_t box[3] = {64, kGemmBN / 2 * kBK * 2 / 128, 1};
+    if (rows > INT32_MAX || !encode_tiled(&p.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                          const_cast<void*>(g.b_packed), 3, dims, strides, box, why))
+      return rows > INT32_MAX ? BI_ERR_INVALID_ARG : BI_ERR_CUDA;
+  } else if (!encode_b(&p.tma_b, g, kGemmBN / 2, why)) {  // K-major: each CTA's columns
     return BI_ERR_CUDA;
   }
   p.c = g.c;
@@ -359,8 +427,8 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   p.N = (int32_t)N;
   p.K = (int32_t)K;
   p.L = (int32_t)L;
-  p.m_tiles = (int32_t)((M + kBM - 1) / kBM);
-  p.n_tiles = (int32_t)((N + kBN - 1) / kBN);
+  p.m_tiles = (int32_t)((M + 2 * kBM - 1) / (2 * kBM));  // 256-row pair tiles
+  p.n_tiles = (int32_t)((N + kGemmBN - 1) / kGemmBN);
   p.k_blocks = (int32_t)((K + kBK - 1) / kBK);
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * L;
   if (tiles > INT32_MAX) {
@@ -375,9 +443,8 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
 
-  const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
-  cudaError_t e = short_a ? launch_rows<kShortARows>(g, p, grid, stream, 8)
-                          : launch_rows<kBM>(g, p, grid, stream, 0);
+  cudaError_t e = short_a ? launch_rows<kShortARows>(g, p, tiles, stream, 8)
+                          : launch_rows<kBM>(g, p, tiles, stream, 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("gemm launch: ") + cudaGetErrorString(e);

@@ -52,6 +52,11 @@ bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, slot).
 cudaError_t set_smem_once(const void* func, int bytes, int slot);
 
+// How many 2-CTA clusters of a kernel compiled with __cluster_dims__(2,1,1)
+// can be resident at once (cudaOccupancyMaxActiveClusters), once per
+// (device, slot); at least 1.
+cudaError_t pair_capacity(const void* func, int threads, int dyn_bytes, int slot, int* pairs);
+
 // A normalised matrix-product problem: c[l] = alpha * a[l] @ b[l] (+ bias).
 struct GemmProblem {
   const void* a;  // bf16, [L][M][K], unit stride on K

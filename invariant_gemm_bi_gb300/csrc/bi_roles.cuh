@@ -14,8 +14,17 @@
 //   * the epilogue computes round(acc * alpha + bias) with separately
 //     rounded fp32 multiply and add, then one conversion to the output type.
 // Which CTA takes which tile (the persistent stride and the raster order)
-// changes nothing in that sequence.  `stride` is the number of CTAs that own
-// tiles: CTA c takes tiles c, c + stride, c + 2*stride, ...
+// changes nothing in that sequence.  `stride` is the number of tile owners
+// (CTAs, or CTA pairs): owner c takes tiles c, c + stride, c + 2*stride, ...
+//
+// PAIR: the GEMM runs on CTA pairs (cta_group::2).  A tile is then 256 x BN:
+// each CTA of the pair stages its own 128 rows of A and half of the tile's BN
+// columns of B, the even CTA issues 128 x 2 = 256-row MMAs that read both
+// CTAs' stages, and each CTA's TMEM receives its own 128 rows x BN columns.
+// Per output element this is the same reduction (same K blocks, same K = 16
+// steps, same order) as above.  BN: the tile's columns (kBN by default); ACC:
+// accumulators in TMEM (the epilogue of one overlaps the main loop of the
+// next ACC - 1 tiles).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -44,7 +53,8 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, int m_tiles, int n_ti
   return {l, first_m + r % gsize, r / gsize};
 }
 
-// Mbarrier addresses of one CTA's pipeline (8 bytes each).
+// Mbarrier addresses of one CTA's pipeline (8 bytes each; tfull / tempty:
+// one per accumulator).
 struct PipeBars {
   uint32_t full0, empty0, tfull0, tempty0, drain;
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return full0 + 8u * s; }
@@ -60,33 +70,38 @@ struct WaitCtl {
 };
 
 // Single thread: issues every UMMA of this CTA's tiles.  Stage s holds
-// A (128 x 64, K-major) at sA + s*A_BYTES and B (kBN x 64) at sB + s*B_BYTES,
-// B either K-major (kBN rows of 128 bytes) or MN-major (kBN/64 chunks of
-// 64 K-rows x 128 bytes, 8 KB apart).
-template <int STAGES, int A_BYTES, int B_BYTES, bool B_MN>
+// A (128 x 64, K-major) at sA + s*A_BYTES and B (BN x 64, with PAIR BN/2 x 64
+// per CTA) at sB + s*B_BYTES, B either K-major (rows of 128 bytes) or MN-major
+// (64-column chunks of 64 K-rows x 128 bytes, 8 KB apart).
+// With PAIR (even CTA only): the same loop with 256-row pair MMAs; stage and
+// accumulator barriers are signalled in both CTAs, and the full / free
+// barriers waited on here also count the peer's arrivals.
+template <int STAGES, int A_BYTES, int B_BYTES, bool B_MN, bool PAIR = false, int BN = kBN,
+          int ACC = 2>
 __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBars& bars,
-                                         uint32_t tmem_base, int num_tiles, int k_blocks,
-                                         int stride, const WaitCtl& w) {
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, B_MN);
+                                         uint32_t tmem_base, int first_tile, int num_tiles,
+                                         int k_blocks, int stride, const WaitCtl& w) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, B_MN);
+  constexpr uint16_t kBoth = 3;
   uint32_t it = 0;
   int local = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += stride, ++local) {
-    const uint32_t buf = local & 1;
-    const uint32_t use = local >> 1;
+  for (int tile = first_tile; ok && tile < num_tiles; tile += stride, ++local) {
+    const uint32_t buf = local % ACC;
+    const uint32_t use = local / ACC;
     if (use > 0 &&
-        !mbar_wait_bounded(bars.tempty(buf), (use - 1) & 1, w.abort, w.status_word, w.limit_ns,
-                           status_code(6, kSiteMmaTmemEmpty))) {
+        !mbar_wait_bounded<PAIR>(bars.tempty(buf), (use - 1) & 1, w.abort, w.status_word, w.limit_ns,
+                                 status_code(6, kSiteMmaTmemEmpty))) {
       ok = false;
       break;
     }
     tc_fence_after_sync();
-    const uint32_t d = tmem_base + buf * kBN;
+    const uint32_t d = tmem_base + buf * BN;
     for (int kb = 0; kb < k_blocks; ++kb, ++it) {
       const uint32_t s = it % STAGES;
       const uint32_t r = it / STAGES;
-      if (!mbar_wait_bounded(bars.full(s), r & 1, w.abort, w.status_word, w.limit_ns,
-                             status_code(6, kSiteMmaFull))) {
+      if (!mbar_wait_bounded<PAIR>(bars.full(s), r & 1, w.abort, w.status_word, w.limit_ns,
+                                   status_code(6, kSiteMmaFull))) {
         ok = false;
         break;
       }
@@ -98,15 +113,29 @@ __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBar
         const uint64_t ad = smem_desc_sw128(a + k * 32, 16, 1024);
         const uint64_t bd = B_MN ? smem_desc_sw128(b + k * 2048, 64 * 128, 1024)
                                  : smem_desc_sw128(b + k * 32, 16, 1024);
-        umma_bf16(d, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        if (PAIR)
+          umma_bf16_pair(d, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        else
+          umma_bf16(d, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
       }
-      umma_commit(bars.empty(s));  // stage s may be refilled once these MMAs finish
+      // stage s may be refilled once these MMAs finish
+      if (PAIR)
+        umma_commit_pair(bars.empty(s), kBoth);
+      else
+        umma_commit(bars.empty(s));
     }
     if (!ok) break;
-    umma_commit(bars.tfull(buf));  // accumulator buf is complete
+    // accumulator buf is complete
+    if (PAIR)
+      umma_commit_pair(bars.tfull(buf), kBoth);
+    else
+      umma_commit(bars.tfull(buf));
   }
   // Every MMA issued above has finished before TMEM can be released.
-  umma_commit(bars.drain);
+  if (PAIR)
+    umma_commit_pair(bars.drain, 1);
+  else
+    umma_commit(bars.drain);
   mbar_wait_bounded(bars.drain, 0, nullptr, w.status_word, w.limit_ns,
                     status_code(6, kSiteDrain));
 }
@@ -115,9 +144,9 @@ __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBar
 //   out[l][m][n] at c + l*c_batch_stride + m*ldc + n,
 //   value = round(acc * alpha (+ bias)), bias either per column n or per
 //   row m (the convolution's output channel, offset by (l % bias_groups)*M).
-// With tma_c set, each warp stages its 32 x 32 chunk in shared memory
-// (swizzled, bank-conflict free) and writes it with a TMA tile store that
-// clips rows >= M and columns >= N; otherwise threads store directly.
+// With tma_c set, each warp whose 32 rows all lie below M stages its 32 x 32
+// chunk in shared memory (swizzled, bank-conflict free) and writes it with a
+// TMA tile store that clips columns >= N; otherwise threads store directly.
 struct OutDesc {
   void* c;
   const void* bias;
@@ -146,19 +175,21 @@ __device__ __forceinline__ float load_bias(const OutDesc& o, int64_t idx) {
 // ready so their latency hides behind the tile's main loop: per row, this
 // thread's row; per column, lane t holds the bias of column t of each
 // 32-column chunk j (broadcast to the warp with shuffles when used).
+template <int BN>
 struct TileBias {
   float row;
-  float col[kBN / 32];
+  float col[BN / 32];
 };
 
+template <int BN>
 __device__ __forceinline__ void load_tile_bias(const OutDesc& o, int l, int m, int n_base, int lane,
-                                               TileBias& tb) {
+                                               TileBias<BN>& tb) {
   if (!o.bias_kind) return;
   if (o.bias_per_row) {
     tb.row = (m < o.M) ? load_bias(o, (int64_t)(l % o.bias_groups) * o.M + m) : 0.0f;
   } else {
 #pragma unroll
-    for (int j = 0; j < kBN / 32; ++j) {
+    for (int j = 0; j < BN / 32; ++j) {
       const int n = n_base + j * 32 + lane;
       tb.col[j] = (n < o.N) ? load_bias(o, n) : 0.0f;
     }
@@ -166,7 +197,8 @@ __device__ __forceinline__ void load_tile_bias(const OutDesc& o, int l, int m, i
 }
 
 // f = acc * alpha (+ bias), each a separately rounded fp32 operation.
-__device__ __forceinline__ void epilogue_math(const OutDesc& o, int j, const TileBias& tb,
+template <int BN>
+__device__ __forceinline__ void epilogue_math(const OutDesc& o, int j, const TileBias<BN>& tb,
                                               const uint32_t (&v)[32], float (&f)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), o.alpha);
@@ -177,7 +209,7 @@ __device__ __forceinline__ void epilogue_math(const OutDesc& o, int j, const Til
     } else {
       float bj = 0.0f;
 #pragma unroll
-      for (int jj = 0; jj < kBN / 32; ++jj)
+      for (int jj = 0; jj < BN / 32; ++jj)
         if (jj == j) bj = tb.col[jj];
 #pragma unroll
       for (int i = 0; i < 32; ++i) f[i] = __fadd_rn(f[i], __shfl_sync(0xffffffffu, bj, i));
@@ -244,13 +276,17 @@ __device__ __forceinline__ void stage_32(const OutDesc& o, uint32_t sbuf, int la
 }
 
 // Converts and stores chunk j (32 columns) of this warp's 32 rows.
-__device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const TileBias& tb,
+template <int BN>
+__device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const TileBias<BN>& tb,
                                                const uint32_t (&v)[32], const TileCoord& tc, int m0,
                                                int lane, uint32_t stage_base, uint32_t& chunk) {
-  const int n0 = tc.nb * kBN + j * 32;
+  const int n0 = tc.nb * BN + j * 32;
   float f[32];
-  epilogue_math(o, j, tb, v, f);
-  if (o.tma_c) {
+  epilogue_math<BN>(o, j, tb, v, f);
+  // A quadrant with rows past M (a decode-sized M, or the last rows of a
+  // problem) stores directly: its few rows do not pay for staging and for
+  // waiting on the staging buffers.  Same values either way.
+  if (o.tma_c && m0 + 32 <= o.M) {
     const uint32_t sbuf = stage_base + (chunk & 1) * kStageOutBytes;
     if (chunk >= 2) {  // the store issued two chunks ago must have read this buffer
       if (lane == 0) bulk_wait_read_1();
@@ -272,28 +308,34 @@ __device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const Ti
 // One warp of the epilogue group: drains TMEM lane quadrant q (rows
 // 32q .. 32q+31 of each tile) for every tile of this CTA.  stage_base: this
 // warp's two staging buffers (used when o.tma_c is set).
+// With PAIR, m_tiles counts 256-row tiles and this CTA (rank `crank` of the
+// pair) drains rows crank*128 .. crank*128+127 of each; the accumulator is
+// released to the even CTA, whose MMA issuer waits for both CTAs.
+template <bool PAIR = false, int BN = kBN, int ACC = 2>
 __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_base,
-                                              const PipeBars& bars, int num_tiles, int m_tiles,
-                                              int n_tiles, int stride, const OutDesc& o,
-                                              uint32_t stage_base, const WaitCtl& w) {
+                                              const PipeBars& bars, int first_tile, int num_tiles,
+                                              int m_tiles, int n_tiles, int stride, const OutDesc& o,
+                                              uint32_t stage_base, const WaitCtl& w,
+                                              uint32_t crank = 0) {
   int local = 0;
   uint32_t chunk = 0;  // staged chunks issued by this warp (selects the buffer)
-  for (int tile = blockIdx.x; tile < num_tiles; tile += stride, ++local) {
-    const uint32_t buf = local & 1;
-    const uint32_t use = local >> 1;
-    const TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
+  for (int tile = first_tile; tile < num_tiles; tile += stride, ++local) {
+    const uint32_t buf = local % ACC;
+    const uint32_t use = local / ACC;
+    TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
+    if (PAIR) tc.mb = 2 * tc.mb + (int)crank;
     const int m0 = tc.mb * kBM + q * 32;
-    TileBias tb;
-    load_tile_bias(o, tc.l, m0 + lane, tc.nb * kBN, lane, tb);
+    TileBias<BN> tb;
+    load_tile_bias<BN>(o, tc.l, m0 + lane, tc.nb * BN, lane, tb);
     const bool ok = mbar_wait_bounded(bars.tfull(buf), use & 1, w.abort, w.status_word,
                                       w.limit_ns, status_code(6, kSiteEpilogueTmemFull));
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after_sync();
-    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kBN;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
     // Chunks holding any output: none when all 32 rows of this quadrant are
     // past M, and none past N.
-    const int n_left = o.N - tc.nb * kBN;
-    const int n_chunks = (m0 < o.M) ? min(kBN / 32, (n_left + 31) / 32) : 0;
+    const int n_left = o.N - tc.nb * BN;
+    const int n_chunks = (m0 < o.M) ? min(BN / 32, (n_left + 31) / 32) : 0;
     // Two register sets: the next chunk's TMEM load is in flight while the
     // current chunk is converted and stored.
     uint32_t va[32], vb[32];
@@ -302,20 +344,25 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     for (int j = 0; j < n_chunks; j += 2) {
       tmem_load_wait(va);
       if (j + 1 < n_chunks) tmem_load_32cols(lane_addr + (j + 1) * 32, vb);
-      epilogue_chunk(o, j, tb, va, tc, m0, lane, stage_base, chunk);
+      epilogue_chunk<BN>(o, j, tb, va, tc, m0, lane, stage_base, chunk);
       if (j + 1 < n_chunks) {
         tmem_load_wait(vb);
         if (j + 2 < n_chunks) tmem_load_32cols(lane_addr + (j + 2) * 32, va);
-        epilogue_chunk(o, j + 1, tb, vb, tc, m0, lane, stage_base, chunk);
+        epilogue_chunk<BN>(o, j + 1, tb, vb, tc, m0, lane, stage_base, chunk);
       }
     }
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars.tempty(buf));
+    if (lane == 0) {
+      if (PAIR && crank != 0)
+        mbar_arrive_remote(bars.tempty(buf), 0);
+      else
+        mbar_arrive(bars.tempty(buf));
+    }
   }
-  // Shared memory must outlive the reads of the stores still in flight, and
-  // the results must be complete when the kernel ends.
-  if (o.tma_c && lane == 0) bulk_wait_all();
+  // Shared memory must outlive the reads of the stores still in flight (the
+  // writes themselves complete before the kernel does).
+  if (o.tma_c && lane == 0) bulk_wait_read_all();
   __syncwarp();
 }
 

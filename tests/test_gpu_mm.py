@@ -252,3 +252,26 @@ def test_short_a_layout_matches_general_layout_bitwise():
         d = a[:32].clone()
         d[1:] = fill
         assert bits_equal(binding.bi_addmm(bias, d, w, out_dtype=torch.float32)[:1], general[:1])
+
+
+# -- tile count vs resident CTA pairs ---------------------------------------
+
+@pytest.mark.parametrize("K", [64, 320, 4096])
+def test_column_count_does_not_change_shared_columns(K):
+    # 38 column tiles leave pairs idle, 76 fill the GPU, 80 make pairs take a
+    # second tile; the columns the three problems share must agree bit for
+    # bit, for plain MN-major and packed weights, with a ragged last tile.
+    a = inputs.normal_bf16((40, K), 1.0, 93).cuda()
+    w = inputs.normal_bf16((K, 256 * 80), 0.02, 94).cuda()
+    bias = inputs.normal_bf16((256 * 80,), 0.01, 95).cuda()
+    widths = (256 * 37 + 72, 256 * 75 + 8, 256 * 80)
+    for M in (1, 29, 40):
+        outs = [binding.bi_addmm(bias[:n], a[:M], w[:, :n], out_dtype=torch.float32) for n in widths]
+        packs = [binding.bi_addmm_packed(bias[:n], a[:M], binding.bi_pack_weight(w[:, :n]),
+                                         out_dtype=torch.float32) for n in widths]
+        for o, pk, n in zip(outs, packs, widths):
+            assert bits_equal(o, outs[-1][:, :n]), (M, n)
+            assert bits_equal(pk, o), (M, n)
+    cols = [0, 1, 256 * 37 + 71, 256 * 75 + 7, 256 * 80 - 1]
+    ref, absum = oracle.mm(a[:3].cpu(), w[:, cols].cpu(), bias=bias[cols].cpu())
+    check_tolerance(outs[-1][:, cols][:3], ref, absum, f"split stream K={K}")
