@@ -349,24 +349,33 @@ def _square(out, binding, inputs, flush_buf, stream, peaks, reps, point):
 
 
 def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
+    # packed filter (bi_conv2d_patch_packed, packed once like the linear weight),
+    # the plain-filter general kernel (bi_conv2d_patch) and cuDNN on the same shapes
     x, wc, bc = inputs.patch_embed(max(inputs.PATCH_EMBED_B), device="cuda")
-    res, y0, yc0 = [], {}, {}
+    wpk = binding.bi_conv_pack_weight(wc)
+    res, y0, yp0, yc0 = [], {}, {}, {}
     for B in inputs.PATCH_EMBED_B:
         xb = x[:B]
         y = torch.empty(B, 1152, 16, 16, dtype=torch.bfloat16, device="cuda")
-        t = measure(lambda: binding.bi_conv2d_patch(xb, wc, bc, stride=14, out=y), flush_buf, stream, reps)
+        t = measure(lambda: binding.bi_conv2d_patch_packed(xb, wpk, bc, out=y), flush_buf, stream, reps)
         y0[B] = y[:1].clone()
         flops = B * (2.0 * 256 * 588 * 1152 + 256 * 1152)
         nb = 2.0 * (B * 3 * 224 * 224 + 1152 * 588 + 1152 + B * 1152 * 256)
         r = {"B": B, **point(flops, nb, t)}
+        tp = measure(lambda: binding.bi_conv2d_patch(xb, wc, bc, stride=14, out=y), flush_buf, stream, reps)
+        yp0[B] = y[:1].clone()
+        r["plain_filter"] = point(flops, nb, tp)
         tc = measure(lambda: F.conv2d(xb, wc, bc, stride=14), flush_buf, stream, reps)
         yc0[B] = F.conv2d(xb, wc, bc, stride=14)[:1].clone()
         r["cudnn_us"] = round(tc * 1e6, 2)
         res.append(r)
     out["patch_embed_conv"] = {"points": res,
+                               "entry_point": "bi_conv2d_patch_packed (plain_filter: bi_conv2d_patch)",
                                "sample0_bit_equal_all_B": all(bits_equal(y0[B], y0[1]) for B in y0),
+                               "plain_filter_sample0_bit_equal_all_B": all(bits_equal(yp0[B], yp0[1])
+                                                                           for B in yp0),
                                "cudnn_sample0_bit_equal_all_B": all(bits_equal(yc0[B], yc0[1]) for B in yc0)}
-    del x, wc, bc
+    del x, wc, bc, wpk
 
 
 def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):

@@ -128,6 +128,53 @@ bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tenso
                           const int32_t dilation[2], int32_t groups, bi_stream stream);
 
 /*
+ * Packed patch-embedding filter, for bi_conv2d_patch_packed.  The filter
+ * w[Co][C][KH][KW] of a non-overlapping patch convolution stored as a
+ * row-major [Co][Kp] bf16 matrix with reduction index
+ *   kp = (ci*KHp + kh)*16 + kw,   KHp = KH rounded up to a multiple of 4,
+ * i.e. every kernel row (ci, kh) padded to 16 slots and every channel to a
+ * multiple of 4 kernel rows; slots with kh >= KH or kw >= KW hold zero.
+ * Packing is a data-layout service for the same convolution, not one of the
+ * pages' operations.
+ */
+typedef struct {
+  void* ptr;              /* device buffer holding the packed filter (caller-owned) */
+  int64_t bytes;          /* its size in bytes */
+  int64_t Co, C, KH, KW;  /* shape of the filter it was packed from */
+  int64_t Kp;             /* row length C * KHp * 16 */
+} bi_conv_packed_weight;
+
+/* Bytes of the packed form of a [Co,C,KH,KW] filter (0 if KW > 16 or empty). */
+int64_t bi_conv_packed_weight_bytes(int64_t Co, int64_t C, int64_t KH, int64_t KW);
+
+/*
+ * Packs w ([Co,C,KH,KW] bf16 contiguous, KW <= 16) into dst (device, 16-byte
+ * aligned, dst_bytes >= bi_conv_packed_weight_bytes(...)); fills *out.
+ * Asynchronous on `stream`.
+ */
+bi_status bi_conv_pack_weight(const bi_tensor* w, void* dst, int64_t dst_bytes,
+                              bi_conv_packed_weight* out, bi_stream stream);
+
+/*
+ * y = conv2d(x, w, bias, stride = (KH, KW), padding 0, dilation 1, groups 1)
+ * -- the patch embedding of "Batch-Invariant VLAs", section "Replacing
+ * nn.Conv2d" -- with w given packed:
+ *   y[b,co,oh,ow] = bias[co] + sum_{ci,kh,kw} x[b, ci, oh*KH+kh, ow*KW+kw] * w[co,ci,kh,kw]
+ * The reduction runs over the packed index kp in ascending order; each
+ * tensor-core K = 16 step is one kernel row (ci, kh) (its zero slots add
+ * exact zeros; image pixels outside a position's own window are never read
+ * into it).  Per output element this is a fixed order, the same for every
+ * batch size, but a different grouping than bi_conv2d_patch's: the two entry
+ * points agree within rounding, not bit for bit.
+ *   x: [B,C,H,W] bf16 contiguous, 16-byte aligned, W a multiple of 8 and
+ *      <= 256;  y: [B,Co,H/KH,W/KW] bf16 or fp32 contiguous, W/KW <= 128;
+ *   bias: [Co] bf16 or fp32, or NULL / ptr == NULL.  Image rows or columns
+ *   past the last whole patch are ignored (as the size formula does).
+ */
+bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_packed_weight* w,
+                                 const bi_tensor* bias, const bi_tensor* y, bi_stream stream);
+
+/*
  * p[r,:] = softmax(s[r,:]) over the last dimension, per row r:
  *   mx = max_j s[r,j];  e_j = expf(s[r,j] - mx);  p[r,j] = e_j * RN(1 / sum_j e_j),
  *   sums in fp32 in a fixed order set by the element index only (4-element

@@ -27,6 +27,7 @@ BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
             "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
+            "bi_conv_packed_weight_bytes", "bi_conv_pack_weight", "bi_conv2d_patch_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
             "bi_last_error_message", "bi_abi_version")
 
@@ -41,6 +42,25 @@ class BiTensor(ctypes.Structure):
 class BiPackedWeightDesc(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("layout", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
+
+
+class BiConvPackedWeightDesc(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_int64), ("Co", ctypes.c_int64),
+                ("C", ctypes.c_int64), ("KH", ctypes.c_int64), ("KW", ctypes.c_int64),
+                ("Kp", ctypes.c_int64)]
+
+
+class ConvPackedWeight:
+    """A patch-embedding filter packed on the device by ``bi_conv_pack_weight``:
+    owns the torch buffer that holds it and the descriptor the library reads."""
+
+    def __init__(self, buffer: torch.Tensor, desc: BiConvPackedWeightDesc):
+        self.buffer = buffer
+        self.desc = desc
+
+    @property
+    def shape(self):
+        return (int(self.desc.Co), int(self.desc.C), int(self.desc.KH), int(self.desc.KW))
 
 
 class PackedWeight:
@@ -94,6 +114,11 @@ def load(path: str | None = None):
                                     ctypes.POINTER(BiPackedWeightDesc), ctypes.c_void_p], st),
                 "bi_addmm_packed": ([ptr, ptr, ctypes.POINTER(BiPackedWeightDesc), ptr,
                                      ctypes.c_void_p], st),
+                "bi_conv_packed_weight_bytes": ([ctypes.c_int64] * 4, ctypes.c_int64),
+                "bi_conv_pack_weight": ([ptr, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.POINTER(BiConvPackedWeightDesc), ctypes.c_void_p], st),
+                "bi_conv2d_patch_packed": ([ptr, ctypes.POINTER(BiConvPackedWeightDesc), ptr, ptr,
+                                            ctypes.c_void_p], st),
                 "bi_device_status": ([ctypes.c_void_p], st),
                 "bi_debug_expire_wait": ([ctypes.c_uint64, ctypes.c_void_p], st),
                 "bi_status_string": ([st], ctypes.c_char_p),
@@ -246,6 +271,39 @@ def bi_addmm_packed(bias: torch.Tensor | None, a: torch.Tensor, b: PackedWeight,
     dbias, da, dc = _desc(bias, "bias"), _desc(a, "a"), _desc(out, "out")
     _check(lib, "bi_addmm_packed",
            lib.bi_addmm_packed(_ref(dbias), _ref(da), ctypes.byref(b.desc), _ref(dc), _stream(stream)))
+    return out
+
+
+def bi_conv_packed_weight_bytes(Co: int, C: int, KH: int, KW: int) -> int:
+    return int(load().bi_conv_packed_weight_bytes(int(Co), int(C), int(KH), int(KW)))
+
+
+def bi_conv_pack_weight(w: torch.Tensor, stream=None) -> ConvPackedWeight:
+    """Packs a [Co, C, KH, KW] bf16 patch-embedding filter (KW <= 16)."""
+    lib = load()
+    Co, C, KH, KW = w.shape
+    nbytes = bi_conv_packed_weight_bytes(Co, C, KH, KW)
+    buf = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=w.device)
+    desc = BiConvPackedWeightDesc()
+    dw_ = _desc(w, "w")
+    _check(lib, "bi_conv_pack_weight",
+           lib.bi_conv_pack_weight(_ref(dw_), ctypes.c_void_p(buf.data_ptr()), nbytes, ctypes.byref(desc),
+                                   _stream(stream)))
+    return ConvPackedWeight(buf, desc)
+
+
+def bi_conv2d_patch_packed(x: torch.Tensor, w: ConvPackedWeight, bias: torch.Tensor | None = None,
+                           out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.bfloat16,
+                           stream=None) -> torch.Tensor:
+    """Non-overlapping patch convolution (stride = kernel size) with a packed filter."""
+    lib = load()
+    Co, C, KH, KW = w.shape
+    if out is None:
+        out = torch.empty((x.shape[0], Co, x.shape[2] // KH, x.shape[3] // KW), dtype=out_dtype,
+                          device=x.device)
+    dx, db, dy = _desc(x, "x"), _desc(bias, "bias"), _desc(out, "out")
+    _check(lib, "bi_conv2d_patch_packed",
+           lib.bi_conv2d_patch_packed(_ref(dx), ctypes.byref(w.desc), _ref(db), _ref(dy), _stream(stream)))
     return out
 
 

@@ -553,6 +553,119 @@ extern "C" bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, con
   return finish(st, why);
 }
 
+// ---------------------------------------------------------------------------
+// Patch convolution with a packed filter
+// ---------------------------------------------------------------------------
+
+extern "C" int64_t bi_conv_packed_weight_bytes(int64_t Co, int64_t C, int64_t KH, int64_t KW) {
+  if (Co <= 0 || C <= 0 || KH <= 0 || KW <= 0 || KW > 16) return 0;
+  return Co * patch_padded_k(C, KH) * 2;
+}
+
+extern "C" bi_status bi_conv_pack_weight(const bi_tensor* w, void* dst, int64_t dst_bytes,
+                                         bi_conv_packed_weight* out, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if ((st = check_tensor(w, "w", 4, &why)) != BI_OK) return finish(st, why);
+  if (w->dtype != BI_BF16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "w must be bf16");
+  if (!out) return finish(BI_ERR_INVALID_ARG, "out: null");
+  const int64_t Co = w->shape[0], C = w->shape[1], KH = w->shape[2], KW = w->shape[3];
+  if (Co < 1 || C < 1 || KH < 1 || KW < 1) return finish(BI_ERR_INVALID_ARG, "empty filter");
+  if (KW > 16) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "packed filters take KW <= 16");
+  if (Co > INT32_MAX || patch_padded_k(C, KH) > INT32_MAX)
+    return finish(BI_ERR_INVALID_ARG, "filter too large");
+  if (!is_contiguous(w)) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "w must be contiguous");
+  const int64_t need = bi_conv_packed_weight_bytes(Co, C, KH, KW);
+  if (!dst || !aligned(dst, 16) || dst_bytes < need)
+    return finish(BI_ERR_INVALID_ARG, "dst must be 16-byte aligned with at least " +
+                                          std::to_string(need) + " bytes");
+  if (!w->ptr || !aligned(w->ptr, 2)) return finish(BI_ERR_INVALID_ARG, "w: null or misaligned data pointer");
+  st = launch_conv_pack(w->ptr, dst, Co, C, KH, KW, (cudaStream_t)stream, &why);
+  if (st == BI_OK) {
+    out->ptr = dst;
+    out->bytes = dst_bytes;
+    out->Co = Co;
+    out->C = C;
+    out->KH = KH;
+    out->KW = KW;
+    out->Kp = patch_padded_k(C, KH);
+  }
+  return finish(st, why);
+}
+
+extern "C" bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_packed_weight* w,
+                                            const bi_tensor* bias, const bi_tensor* y,
+                                            bi_stream stream) {
+  std::string why;
+  bi_status st;
+  auto fail = [&](bi_status s, const std::string& m) {
+    why = m;
+    return finish(s, why);
+  };
+  if ((st = check_tensor(x, "x", 4, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(y, "y", 4, &why)) != BI_OK) return finish(st, why);
+  if (!w || !w->ptr) return fail(BI_ERR_INVALID_ARG, "packed filter: null");
+  if (x->dtype != BI_BF16) return fail(BI_ERR_UNSUPPORTED_DTYPE, "x must be bf16");
+  if (y->dtype != BI_BF16 && y->dtype != BI_F32) return fail(BI_ERR_UNSUPPORTED_DTYPE, "y must be bf16 or fp32");
+  const int64_t Co = w->Co, C = w->C, KH = w->KH, KW = w->KW;
+  if (Co < 1 || C < 1 || KH < 1 || KW < 1 || KW > 16 || w->Kp != patch_padded_k(C, KH) ||
+      w->bytes < bi_conv_packed_weight_bytes(Co, C, KH, KW) || !aligned(w->ptr, 16))
+    return fail(BI_ERR_INVALID_ARG, "packed filter descriptor is inconsistent");
+  const int64_t B = x->shape[0], H = x->shape[2], W = x->shape[3];
+  if (x->shape[1] != C) return fail(BI_ERR_SHAPE_MISMATCH, "x has " + std::to_string(x->shape[1]) +
+                                                               " channels, the filter " + std::to_string(C));
+  const int64_t Ho = H / KH, Wo = W / KW;
+  if (y->shape[0] != B || y->shape[1] != Co || y->shape[2] != Ho || y->shape[3] != Wo)
+    return fail(BI_ERR_SHAPE_MISMATCH, "y must be [B, Co, H/KH, W/KW] = [" + std::to_string(B) + ", " +
+                                           std::to_string(Co) + ", " + std::to_string(Ho) + ", " +
+                                           std::to_string(Wo) + "]");
+  if (!is_contiguous(x) || !is_contiguous(y))
+    return fail(BI_ERR_UNSUPPORTED_LAYOUT, "x and y must be contiguous (NCHW)");
+  int bias_kind = 0;
+  if (bias && bias->ptr) {
+    if ((st = check_tensor(bias, "bias", 1, &why)) != BI_OK) return finish(st, why);
+    if (bias->shape[0] != Co) return fail(BI_ERR_SHAPE_MISMATCH, "bias must have Co elements");
+    if (bias->stride[0] != 1 && Co > 1) return fail(BI_ERR_UNSUPPORTED_LAYOUT, "bias must be contiguous");
+    if (bias->dtype == BI_BF16)
+      bias_kind = 1;
+    else if (bias->dtype == BI_F32)
+      bias_kind = 2;
+    else
+      return fail(BI_ERR_UNSUPPORTED_DTYPE, "bias must be bf16 or fp32");
+  }
+  if (B == 0 || Ho == 0 || Wo == 0) return finish(BI_OK, why);
+  // The image is read as whole rows by TMA: 16-byte rows, at most 256 wide,
+  // and one K block's rows (4 kernel rows of each output row of a tile) must
+  // fit one staging buffer.
+  const int64_t t_oh = std::min<int64_t>(Ho, 128 / std::max<int64_t>(Wo, 1));
+  if ((W * 2) % 16 != 0 || W > 256 || Wo > 128 || W * 4 * t_oh * 2 > kPatchStageMax)
+    return fail(BI_ERR_UNSUPPORTED_LAYOUT,
+                "image rows must be a multiple of 8 and at most 256 elements, with W/KW <= 128");
+  if (!x->ptr || !y->ptr) return fail(BI_ERR_INVALID_ARG, "null data pointer");
+  if (!aligned(x->ptr, 16) || !aligned(y->ptr, y->dtype == BI_F32 ? 4 : 2))
+    return fail(BI_ERR_UNSUPPORTED_LAYOUT, "x must be 16-byte aligned, y aligned to its element size");
+  if (B * C > INT32_MAX || Ho * Wo > INT32_MAX) return fail(BI_ERR_INVALID_ARG, "problem too large");
+  PatchProblem pp;
+  memset(&pp, 0, sizeof(pp));
+  pp.x = x->ptr;
+  pp.wp = w->ptr;
+  pp.bias = bias_kind ? bias->ptr : nullptr;
+  pp.bias_kind = bias_kind;
+  pp.y = y->ptr;
+  pp.out_f32 = y->dtype == BI_F32;
+  pp.B = B;
+  pp.C = C;
+  pp.H = H;
+  pp.W = W;
+  pp.Co = Co;
+  pp.KH = KH;
+  pp.KW = KW;
+  pp.Ho = Ho;
+  pp.Wo = Wo;
+  st = launch_patch(pp, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
 extern "C" bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
   std::string why;
   bi_status st;
@@ -629,4 +742,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 2; }
+extern "C" int32_t bi_abi_version(void) { return 3; }

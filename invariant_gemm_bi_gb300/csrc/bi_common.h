@@ -86,6 +86,25 @@ struct ConvParams {
   uint64_t wait_limit_ns;
 };
 
+// Largest staged K block of image rows of the patch convolution (4 kernel
+// rows x t_oh output rows x the image width, bf16).
+constexpr int kPatchStageMax = 32768;
+
+// Non-overlapping patch convolution with a packed filter (see bi_patch.cu).
+struct PatchParams {
+  CUtensorMap tma_x;  // x as {W, KH, Ho, B*C}, box {W, 4, t_oh, 1}, no swizzle
+  CUtensorMap tma_w;  // packed filter [Co][Kp], box {64, BN, 1}, 128B swizzle
+  const void* bias;   // [Co] or null
+  void* y;            // [B][Co][Ho][Wo] contiguous
+  int32_t C, W, KW, Wo, khq;    // khq: K blocks per input channel (KH rounded up to 4, / 4)
+  int32_t t_oh, tile_rows, P, Co;  // output rows per tile, positions per tile, Ho*Wo
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles;
+  uint32_t stg_bytes;  // bytes of one staged K block of image rows (W * 4 * t_oh * 2)
+  int32_t out_f32, bias_kind;
+  unsigned int* status_word;
+  uint64_t wait_limit_ns;
+};
+
 struct SoftmaxParams {
   const float* s;
   void* p;

@@ -378,6 +378,8 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
     o.vec_store = p.vec_store;
     o.bias_per_row = 1;
     o.bias_groups = p.groups;
+    o.trans = 0;
+    o.tile_rows = kBM;
     o.tma_c = p.use_tma_store ? &p.tma_y : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 5) * 2 * kStageOutBytes;
     epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,

@@ -244,6 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     o.vec_store = p.vec_store;
     o.bias_per_row = 0;
     o.bias_groups = 1;
+    o.trans = 0;
+    o.tile_rows = kBM;
     o.tma_c = (Lay::STAGING_BYTES > 0 && p.use_tma_store) ? &p.tma_c : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 2) * 2 * kStageOutBytes;
     epilogue_role<true, kGemmBN, kGemmAcc>(warp & 3, lane, tmem_base, bars, first_tile, p.num_tiles, p.m_tiles,

@@ -95,6 +95,22 @@ struct ConvProblem {
 
 bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* why);
 
+// Non-overlapping patch convolution with a packed filter (bi_patch.cu).
+struct PatchProblem {
+  const void* x;   // [B][C][H][W] bf16 contiguous, 16-byte aligned, W*2 % 16 == 0
+  const void* wp;  // packed filter [Co][patch_padded_k(C, KH)]
+  const void* bias;
+  int bias_kind;
+  void* y;  // [B][Co][Ho][Wo] contiguous
+  int out_f32;
+  int64_t B, C, H, W, Co, KH, KW, Ho, Wo;
+};
+// Row length of the packed filter: C * (KH rounded up to 4) * 16.
+int64_t patch_padded_k(int64_t C, int64_t KH);
+bi_status launch_conv_pack(const void* w, void* dst, int64_t Co, int64_t C, int64_t KH, int64_t KW,
+                           cudaStream_t stream, std::string* why);
+bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string* why);
+
 bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::string* why);
 
 bi_status launch_fill_bias(const GemmProblem& g, cudaStream_t stream, std::string* why);

@@ -1,0 +1,373 @@
+// bi_patch.cu -- non-overlapping patch convolution (patch embedding) as an
+// implicit-im2col tcgen05 GEMM with a packed filter.
+//
+// For stride = kernel size, no padding, no dilation and one group (the
+// patch-embedding layer of "Batch-Invariant VLAs", section "Replacing
+// nn.Conv2d", and "Batch-Invariant Kernel Design: Conv2d and Attention BMM",
+// section "Kernel 1: Conv2d"), output position (oh, ow) of sample b reads the
+// disjoint KH x KW window of every channel at (oh*KH, ow*KW).  Per sample
+//   Y[b]^T (P x Co) = Patches[b] (P x Kp) . Wp^T (Kp x Co)  + bias
+// with P = Ho*Wo positions as the rows of the product.  The reduction runs
+// over kp = (ci*KHp + kh)*16 + kw, KHp = KH rounded up to a multiple of 4:
+// every kernel row (ci, kh) occupies 16 slots, slots kh >= KH or kw >= KW
+// are zero on both sides.  One tensor-core K = 16 step is thus one kernel row,
+// and a 64-wide K block is four rows (ci, kh0 .. kh0+3) of one channel.
+//
+// No unfolded matrix exists anywhere.  Per K block the producer TMA-loads,
+// for the tile's t_oh output rows, the four image rows (ci, oh*KH + kh0 ..
+// +3) of the sample -- whole rows, 16-byte aligned, rows past KH zero-filled
+// by the copy engine -- and the [256 x 64] block of the packed filter.  Four
+// warps then rebuild the K-major, 128-byte-swizzled patch tile (one tile row
+// per output position) from the staged rows in shared memory, writing zeros
+// for kw >= KW; the UMMA issue loop and the epilogue are the GEMM's.  A tile
+// is (sample, block of t_oh output rows, 256 channels): it never mixes
+// samples, so one sample's arithmetic is the same for every batch size.
+//
+//   warp 0      producer: image rows (staging ring) and filter blocks (TMA)
+//   warp 1      TMEM allocator + UMMA issuer (128 x 256 x 16, cta_group::1)
+//   warps 2..5  epilogue: tcgen05.ld -> + bias -> rounding -> y (NCHW: the
+//               32 threads of a warp write 32 consecutive positions of a
+//               channel per store)
+//   warps 6..9  patch-tile builders
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bi_common.h"
+#include "bi_launch.h"
+#include "bi_ptx.cuh"
+#include "bi_roles.cuh"
+
+namespace bi {
+
+struct PatchLayout {
+  static constexpr int A_BYTES = kBM * kBK * 2;  // 128 positions x 64 k
+  static constexpr int B_BYTES = kBN * kBK * 2;  // 256 channels x 64 k
+  static constexpr int STAGES = 3;
+  static constexpr int STG_BUFS = 2;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int DYN_BYTES =
+      1024 + STAGES * (A_BYTES + B_BYTES) + STG_BUFS * kPatchStageMax + BAR_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * kBN;
+  static_assert(DYN_BYTES <= 232448, "fits the opt-in shared memory of one CTA");
+  static_assert(DYN_BYTES > 116 * 1024, "one CTA per SM: TMEM is allocated whole");
+  static_assert(8 * (2 * STAGES + 2 * STG_BUFS + 5) + 8 <= BAR_BYTES, "barriers fit their block");
+};
+
+constexpr int kPatchThreads = 320;
+constexpr int kPatchBuilders = 128;  // warps 6..9
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
+// K-major tile (rows of 64 bf16).
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Builds tile row r (one output position, or zeros past the tile's positions)
+// of K block `kb` from the staged image rows: chunk 2g+h holds kw = 8h .. 8h+7
+// of kernel row kh0 + g.  Staged layout: [oh_l][g][x], x over the image width.
+__device__ __forceinline__ void build_patch_row(const PatchParams& p, uint32_t a_dst, uint32_t stg,
+                                                int r) {
+  uint32_t v[8][4];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) v[c][0] = v[c][1] = v[c][2] = v[c][3] = 0u;
+  if (r < p.tile_rows) {
+    const int oh_l = r / p.Wo;
+    const int ow = r - oh_l * p.Wo;
+    if ((p.KW & 1) == 0) {
+      // Even KW: every staged pair (kw, kw+1) with kw < KW is 4-byte aligned
+      // and lies inside its image row; pairs past KW are not read.
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (2 * e < p.KW) {
+            uint32_t w;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(row + 4 * e));
+            v[2 * g + (e >> 2)][e & 3] = w;
+          }
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (e < p.KW) {
+            uint16_t h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(row + 2 * e));
+            v[2 * g + (e >> 3)][(e & 7) >> 1] |= (uint32_t)h << (16 * (e & 1));
+          }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) st_shared_v4(a_dst + sw128_chunk(r, c), v[c][0], v[c][1], v[c][2], v[c][3]);
+}
+
+__global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_constant__ PatchParams p) {
+  using Lay = PatchLayout;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = sA + Lay::STAGES * Lay::A_BYTES;
+  const uint32_t sStg = sB + Lay::STAGES * Lay::B_BYTES;
+  const uint32_t bar0 = sStg + Lay::STG_BUFS * kPatchStageMax;
+  PipeBars bars;
+  bars.full0 = bar0;
+  bars.empty0 = bar0 + 8 * Lay::STAGES;
+  bars.tfull0 = bars.empty0 + 8 * Lay::STAGES;
+  bars.tempty0 = bars.tfull0 + 16;
+  bars.drain = bars.tempty0 + 16;
+  const uint32_t stg_full0 = bars.drain + 8;
+  const uint32_t stg_empty0 = stg_full0 + 8 * Lay::STG_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (stg_empty0 + 8 * Lay::STG_BUFS - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    // A stage is full when its filter block has landed and the four builder
+    // warps have written its patch tile.
+    for (int s = 0; s < Lay::STAGES; ++s) {
+      mbar_init(bars.full(s), 1 + kPatchBuilders / 32);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int q = 0; q < Lay::STG_BUFS; ++q) {
+      mbar_init(stg_full0 + 8 * q, 1);
+      mbar_init(stg_empty0 + 8 * q, kPatchBuilders / 32);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.tfull(b), 1);
+      mbar_init(bars.tempty(b), 4);
+    }
+    mbar_init(bars.drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&p.tma_x);
+    tma_prefetch_desc(&p.tma_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.status_word, p.wait_limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(tile, p.m_tiles, p.n_tiles);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
+          const uint32_t q = it % Lay::STG_BUFS, rq = it / Lay::STG_BUFS;
+          if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
+                                          wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
+            ok = false;
+            break;
+          }
+          if (rq > 0 && !mbar_wait_bounded(stg_empty0 + 8 * q, (rq - 1) & 1, wc.abort, wc.status_word,
+                                           wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bars.full(s), Lay::B_BYTES);
+          tma_load_3d(sB + s * Lay::B_BYTES, &p.tma_w, bars.full(s), kb * kBK, tc.nb * kBN, 0);
+          const int ci = kb / p.khq;
+          const int kh0 = (kb - ci * p.khq) * 4;
+          mbar_arrive_expect_tx(stg_full0 + 8 * q, p.stg_bytes);
+          tma_load_4d(sStg + q * kPatchStageMax, &p.tma_x, stg_full0 + 8 * q, 0, kh0, tc.mb * p.t_oh,
+                      tc.l * p.C + ci);
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits.
+      const uint32_t first = it > (uint32_t)Lay::STAGES ? it - Lay::STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        if (!mbar_wait_bounded(bars.full(j % Lay::STAGES), (j / Lay::STAGES) & 1, nullptr,
+                               wc.status_word, wc.limit_ns, status_code(6, kSiteDrain)))
+          break;
+      const uint32_t first_q = it > (uint32_t)Lay::STG_BUFS ? it - Lay::STG_BUFS : 0u;
+      for (uint32_t j = first_q; j < it; ++j)
+        if (!mbar_wait_bounded(stg_full0 + 8 * (j % Lay::STG_BUFS), (j / Lay::STG_BUFS) & 1, nullptr,
+                               wc.status_word, wc.limit_ns, status_code(6, kSiteDrain)))
+          break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0)
+      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, false>(
+          sA, sB, bars, tmem_base, blockIdx.x, p.num_tiles, p.k_blocks, gridDim.x, wc);
+  } else if (warp < 6) {
+    OutDesc o;
+    o.c = p.y;
+    o.bias = p.bias;
+    o.tma_c = nullptr;
+    o.ldc = p.P;  // between output channels (the tile's columns)
+    o.c_batch_stride = (int64_t)p.Co * p.P;
+    o.bias_stride = 1;
+    o.alpha = 1.0f;
+    o.M = p.P;
+    o.N = p.Co;
+    o.out_f32 = p.out_f32;
+    o.bias_kind = p.bias_kind;
+    o.vec_store = 0;
+    o.bias_per_row = 0;
+    o.bias_groups = 1;
+    o.trans = 1;
+    o.tile_rows = p.tile_rows;
+    epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,
+                  gridDim.x, o, 0u, wc);
+  } else {
+    // Patch-tile builders: thread t writes tile row t of every K block.
+    const int t = threadIdx.x - 6 * 32;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
+        const uint32_t q = it % Lay::STG_BUFS, rq = it / Lay::STG_BUFS;
+        bool got = mbar_wait_bounded(stg_full0 + 8 * q, rq & 1, wc.abort, wc.status_word, wc.limit_ns,
+                                     status_code(6, kSiteConvProducer));
+        if (got && r > 0)
+          got = mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word, wc.limit_ns,
+                                  status_code(6, kSiteConvProducer));
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        build_patch_row(p, sA + s * Lay::A_BYTES, sStg + q * kPatchStageMax, t);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bars.full(s));
+          mbar_arrive(stg_empty0 + 8 * q);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Lay::TMEM_COLS);
+  }
+}
+
+// Packed filter: wp[co][kp], kp = (ci*KHp + kh)*16 + kw, zero where kh >= KH
+// or kw >= KW.  One thread per 8 consecutive kp (16-byte stores).
+__global__ void conv_pack_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ wp, int Co, int C,
+                                 int KH, int KW, int KHp, int Kp) {
+  const int64_t groups = (int64_t)Co * (Kp / 8);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < groups;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int co = (int)(i / (Kp / 8));
+    const int kp0 = (int)(i - (int64_t)co * (Kp / 8)) * 8;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int kp = kp0 + e;
+      const int kw = kp & 15;
+      const int kh = (kp >> 4) % KHp;
+      const int ci = (kp >> 4) / KHp;
+      if (kh < KH && kw < KW)
+        v[e >> 1] |= (uint32_t)w[(((int64_t)co * C + ci) * KH + kh) * KW + kw] << (16 * (e & 1));
+    }
+    *reinterpret_cast<uint4*>(wp + (int64_t)co * Kp + kp0) = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+int64_t patch_padded_k(int64_t C, int64_t KH) { return C * ((KH + 3) / 4 * 4) * 16; }
+
+bi_status launch_conv_pack(const void* w, void* dst, int64_t Co, int64_t C, int64_t KH, int64_t KW,
+                           cudaStream_t stream, std::string* why) {
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, why);
+  if (st != BI_OK) return st;
+  const int64_t Kp = patch_padded_k(C, KH);
+  const int64_t groups = Co * (Kp / 8);
+  const int grid = (int)std::min<int64_t>((groups + 255) / 256, (int64_t)dev.num_sms * 8);
+  conv_pack_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(w),
+                                             reinterpret_cast<uint16_t*>(dst), (int)Co, (int)C, (int)KH,
+                                             (int)KW, (int)((KH + 3) / 4 * 4), (int)Kp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("conv pack launch: ") + cudaGetErrorString(e);
+    return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
+bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string* why) {
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, why);
+  if (st != BI_OK) return st;
+  PatchParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t Kp = patch_padded_k(pp.C, pp.KH);
+  const int64_t t_oh = std::min<int64_t>(pp.Ho, kBM / pp.Wo);
+  // x as {W, KH, Ho, B*C}: element (x, kh, oh, b*C + ci) is x[b][ci][oh*KH + kh][x].
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)pp.W, (cuuint64_t)pp.KH, (cuuint64_t)pp.Ho,
+                                (cuuint64_t)(pp.B * pp.C)};
+    const cuuint64_t strides[3] = {(cuuint64_t)pp.W * 2, (cuuint64_t)(pp.KH * pp.W * 2),
+                                   (cuuint64_t)(pp.H * pp.W * 2)};
+    const cuuint32_t box[4] = {(cuuint32_t)pp.W, 4, (cuuint32_t)t_oh, 1};
+    if (!encode_tiled(&p.tma_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      const_cast<void*>(pp.x), 4, dims, strides, box, why))
+      return BI_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)Kp, (cuuint64_t)pp.Co, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)Kp * 2, (cuuint64_t)(Kp * 2 * pp.Co)};
+    const cuuint32_t box[3] = {kBK, kBN, 1};
+    if (!encode_tiled_bf16(&p.tma_w, const_cast<void*>(pp.wp), 3, dims, strides, box, why))
+      return BI_ERR_CUDA;
+  }
+  p.bias = pp.bias;
+  p.y = pp.y;
+  p.C = (int32_t)pp.C;
+  p.W = (int32_t)pp.W;
+  p.KW = (int32_t)pp.KW;
+  p.Wo = (int32_t)pp.Wo;
+  p.khq = (int32_t)((pp.KH + 3) / 4);
+  p.t_oh = (int32_t)t_oh;
+  p.tile_rows = (int32_t)(t_oh * pp.Wo);
+  p.P = (int32_t)(pp.Ho * pp.Wo);
+  p.Co = (int32_t)pp.Co;
+  p.m_tiles = (int32_t)((pp.Ho + t_oh - 1) / t_oh);
+  p.n_tiles = (int32_t)((pp.Co + kBN - 1) / kBN);
+  p.k_blocks = (int32_t)(Kp / kBK);
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * pp.B;
+  if (tiles > INT32_MAX) {
+    *why = "tile count exceeds 2^31";
+    return BI_ERR_INVALID_ARG;
+  }
+  p.num_tiles = (int32_t)tiles;
+  p.stg_bytes = (uint32_t)(pp.W * 4 * t_oh * 2);
+  p.out_f32 = pp.out_f32;
+  p.bias_kind = pp.bias_kind;
+  p.status_word = dev.status_word;
+  p.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&patch_kernel), PatchLayout::DYN_BYTES, 6);
+  if (e == cudaSuccess) {
+    const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
+    patch_kernel<<<grid, kPatchThreads, PatchLayout::DYN_BYTES, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    *why = std::string("patch conv launch: ") + cudaGetErrorString(e);
+    return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
+}  // namespace bi

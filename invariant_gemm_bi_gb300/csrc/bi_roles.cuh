@@ -140,8 +140,10 @@ __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBar
                     status_code(6, kSiteDrain));
 }
 
-// Output addressing shared by the GEMM and the convolution:
-//   out[l][m][n] at c + l*c_batch_stride + m*ldc + n,
+// Output addressing shared by the GEMM and the convolutions:
+//   out[l][m][n] at c + l*c_batch_stride + m*ldc + n, or with `trans` at
+//   c + l*c_batch_stride + n*ldc + m (the patch convolution, whose tile rows
+//   are output positions and columns output channels),
 //   value = round(acc * alpha (+ bias)), bias either per column n or per
 //   row m (the convolution's output channel, offset by (l % bias_groups)*M).
 // With tma_c set, each warp whose 32 rows all lie below M stages its 32 x 32
@@ -156,6 +158,10 @@ struct OutDesc {
   int32_t M, N;
   int32_t out_f32, bias_kind, vec_store;
   int32_t bias_per_row, bias_groups;
+  int32_t trans;
+  // Tile row r of m block mb is output row mb*tile_rows + r, and only rows
+  // r < tile_rows are outputs (kBM except for the patch convolution).
+  int32_t tile_rows;
 };
 
 // Epilogue staging: per epilogue warp, two 4 KB buffers (double-buffered
@@ -222,10 +228,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Thread owns output row m and 32 consecutive columns starting at n0.
-__device__ __forceinline__ void store_32_direct(const OutDesc& o, int l, int m, int n0,
+// Thread owns output row m and 32 consecutive columns starting at n0 (row_ok:
+// the thread's tile row is an output row).
+__device__ __forceinline__ void store_32_direct(const OutDesc& o, int l, int m, int n0, bool row_ok,
                                                 const float (&f)[32]) {
-  if (m >= o.M || n0 >= o.N) return;
+  if (!row_ok || m >= o.M || n0 >= o.N) return;
+  if (o.trans) {
+    // Column n of the tile is output row n: a warp's 32 threads (consecutive
+    // m) write 32 consecutive elements of it per column.
+    const int64_t base = (int64_t)l * o.c_batch_stride + m;
+    if (o.out_f32) {
+      float* dst = reinterpret_cast<float*>(o.c) + base;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < o.N) dst[(int64_t)(n0 + i) * o.ldc] = f[i];
+    } else {
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.c) + base;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (n0 + i < o.N) dst[(int64_t)(n0 + i) * o.ldc] = __float2bfloat16_rn(f[i]);
+    }
+    return;
+  }
   const int64_t off = (int64_t)l * o.c_batch_stride + (int64_t)m * o.ldc + n0;
   const bool full = o.vec_store && (n0 + 32 <= o.N);
   if (o.out_f32) {
@@ -279,7 +303,8 @@ __device__ __forceinline__ void stage_32(const OutDesc& o, uint32_t sbuf, int la
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const TileBias<BN>& tb,
                                                const uint32_t (&v)[32], const TileCoord& tc, int m0,
-                                               int lane, uint32_t stage_base, uint32_t& chunk) {
+                                               int lane, bool row_ok, uint32_t stage_base,
+                                               uint32_t& chunk) {
   const int n0 = tc.nb * BN + j * 32;
   float f[32];
   epilogue_math<BN>(o, j, tb, v, f);
@@ -301,7 +326,7 @@ __device__ __forceinline__ void epilogue_chunk(const OutDesc& o, int j, const Ti
     }
     ++chunk;
   } else {
-    store_32_direct(o, tc.l, m0 + lane, n0, f);
+    store_32_direct(o, tc.l, m0 + lane, n0, row_ok, f);
   }
 }
 
@@ -324,7 +349,9 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     const uint32_t use = local / ACC;
     TileCoord tc = decode_tile(tile, m_tiles, n_tiles);
     if (PAIR) tc.mb = 2 * tc.mb + (int)crank;
-    const int m0 = tc.mb * kBM + q * 32;
+    const int r0 = q * 32;
+    const int m0 = tc.mb * o.tile_rows + r0;
+    const bool row_ok = r0 + lane < o.tile_rows;
     TileBias<BN> tb;
     load_tile_bias<BN>(o, tc.l, m0 + lane, tc.nb * BN, lane, tb);
     const bool ok = mbar_wait_bounded(bars.tfull(buf), use & 1, w.abort, w.status_word,
@@ -335,7 +362,7 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     // Chunks holding any output: none when all 32 rows of this quadrant are
     // past M, and none past N.
     const int n_left = o.N - tc.nb * BN;
-    const int n_chunks = (m0 < o.M) ? min(BN / 32, (n_left + 31) / 32) : 0;
+    const int n_chunks = (r0 < o.tile_rows && m0 < o.M) ? min(BN / 32, (n_left + 31) / 32) : 0;
     // Two register sets: the next chunk's TMEM load is in flight while the
     // current chunk is converted and stored.
     uint32_t va[32], vb[32];
@@ -344,11 +371,11 @@ __device__ __forceinline__ void epilogue_role(int q, int lane, uint32_t tmem_bas
     for (int j = 0; j < n_chunks; j += 2) {
       tmem_load_wait(va);
       if (j + 1 < n_chunks) tmem_load_32cols(lane_addr + (j + 1) * 32, vb);
-      epilogue_chunk<BN>(o, j, tb, va, tc, m0, lane, stage_base, chunk);
+      epilogue_chunk<BN>(o, j, tb, va, tc, m0, lane, row_ok, stage_base, chunk);
       if (j + 1 < n_chunks) {
         tmem_load_wait(vb);
         if (j + 2 < n_chunks) tmem_load_32cols(lane_addr + (j + 2) * 32, va);
-        epilogue_chunk<BN>(o, j + 1, tb, vb, tc, m0, lane, stage_base, chunk);
+        epilogue_chunk<BN>(o, j + 1, tb, vb, tc, m0, lane, row_ok, stage_base, chunk);
       }
     }
     tc_fence_before_sync();

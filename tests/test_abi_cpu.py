@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 2
+    assert lib.bi_abi_version() == 3
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -170,3 +170,45 @@ def test_packed_weight_size_and_validation(lib):
     pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 256)
     st = lib.bi_addmm_packed(None, _r(_t([4, 128])), ctypes.byref(pd), _r(_t([4, 256], dtype=2)), None)
     assert st == binding.BI_ERR_SHAPE_MISMATCH
+
+
+def test_conv_packed_weight_size_and_validation(lib):
+    # [Co][C * (KH rounded up to 4) * 16] bf16
+    assert lib.bi_conv_packed_weight_bytes(1152, 3, 14, 14) == 1152 * 3 * 16 * 16 * 2
+    assert lib.bi_conv_packed_weight_bytes(8, 2, 5, 3) == 8 * 2 * 8 * 16 * 2
+    assert lib.bi_conv_packed_weight_bytes(8, 2, 5, 17) == 0
+    assert lib.bi_conv_packed_weight_bytes(0, 2, 5, 3) == 0
+    desc = binding.BiConvPackedWeightDesc()
+    big = 1 << 24
+    # fp32 filter refused; KW > 16 refused; too-small destination refused
+    assert lib.bi_conv_pack_weight(_r(_t([8, 3, 4, 4], dtype=2)), FAKE, big, ctypes.byref(desc),
+                                   None) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert lib.bi_conv_pack_weight(_r(_t([8, 3, 4, 17])), FAKE, big, ctypes.byref(desc),
+                                   None) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert lib.bi_conv_pack_weight(_r(_t([8, 3, 4, 4])), FAKE, 64, ctypes.byref(desc),
+                                   None) == binding.BI_ERR_INVALID_ARG
+    # the convolution itself: a consistent descriptor of a [1152, 3, 14, 14] filter
+    pw = binding.BiConvPackedWeightDesc(FAKE, big, 1152, 3, 14, 14, 3 * 16 * 16)
+    x = _t([2, 3, 224, 224])
+    y = _t([2, 1152, 16, 16])
+
+    def conv(x_, pw_, y_):
+        return lib.bi_conv2d_patch_packed(_r(x_), ctypes.byref(pw_), None, _r(y_), None)
+
+    # channel count differs from the filter's
+    assert conv(_t([2, 4, 224, 224]), pw, y) == binding.BI_ERR_SHAPE_MISMATCH
+    # output extent not [B, Co, H/KH, W/KW]
+    assert conv(x, pw, _t([2, 1152, 16, 15])) == binding.BI_ERR_SHAPE_MISMATCH
+    # image rows not a multiple of 8 elements (TMA reads whole 16-byte rows)
+    assert conv(_t([2, 3, 224, 230]), pw, y) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # image wider than one staged row
+    assert conv(_t([1, 3, 14, 264]), pw, _t([1, 1152, 1, 18])) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # misaligned image base
+    assert conv(_t([2, 3, 224, 224], ptr=FAKE + 2), pw, y) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # descriptor whose row length does not match its shape
+    bad = binding.BiConvPackedWeightDesc(FAKE, big, 1152, 3, 14, 14, 588)
+    assert conv(x, bad, y) == binding.BI_ERR_INVALID_ARG
+    # bf16 / fp32 only for y
+    assert conv(x, pw, _t([2, 1152, 16, 16], dtype=1)) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # nothing to compute: OK before any CUDA call
+    assert conv(_t([0, 3, 224, 224]), pw, _t([0, 1152, 16, 16])) == binding.BI_OK
