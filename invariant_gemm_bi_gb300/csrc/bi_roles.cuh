@@ -6,7 +6,9 @@
 // Doesn't Mean Deterministic LLM Inference", section "Why This Achieves Batch
 // Invariance": fixed block sizes, one core owns a tile's whole reduction, the
 // K tiles always in the same order, no split-K):
-//   * every output tile is 128 x kBN and is reduced by exactly one CTA;
+//   * every output tile has one fixed shape per kernel (GEMM: 256 x 256 on a
+//     CTA pair; convolutions: 128 x 256 on one CTA) and is reduced by
+//     exactly one CTA (pair);
 //   * its K reduction is K blocks of 64 in ascending order, each issued as
 //     four tcgen05.mma steps of K = 16 in ascending order into one fp32 TMEM
 //     accumulator, the first step overwriting (accumulator starts from the
