@@ -307,6 +307,8 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -
         _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
     if want("tiny"):
         _tiny(out, binding, inputs, flush_buf, stream, reps)
+    if want("fp16"):
+        _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
     return out
 
 
@@ -346,6 +348,27 @@ def _square(out, binding, inputs, flush_buf, stream, peaks, reps, point):
                         "cublas_row0_bit_equal_all_M": all(bits_equal(rows0[("cublas", M)], rows0[("cublas", 1)])
                                                            for M in inputs.SQUARE_MM_M)}
     del a, w, wp
+
+
+def _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point):
+    # the LLM-linear layer with fp16 operands and output (packed weight), its
+    # own fixed fp16 tile path; cuBLAS fp16 addmm alongside
+    x, w, bias = inputs.llm_addmm_f16(max(inputs.LLM_ADDMM_F16_M), device="cuda")
+    wp = binding.bi_pack_weight(w)
+    res, rows0 = [], {}
+    for M in inputs.LLM_ADDMM_F16_M:
+        xm = x[:M]
+        c = torch.empty(M, N_DIM, dtype=torch.float16, device="cuda")
+        t = measure(lambda: binding.bi_addmm_packed(bias, xm, wp, out=c), flush_buf, stream, reps)
+        rows0[M] = c[:1].clone()
+        r = {"M": M, **point(addmm_flops(M), addmm_bytes(M), t)}
+        r["cublas_us"] = round(measure(lambda: torch.addmm(bias, xm, w), flush_buf, stream, reps) * 1e6, 2)
+        res.append(r)
+        del c
+    first = inputs.LLM_ADDMM_F16_M[0]
+    out["llm_addmm_fp16"] = {"points": res,
+                             "row0_bit_equal_all_M": all(bits_equal(rows0[M], rows0[first]) for M in rows0)}
+    del x, w, bias, wp
 
 
 def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
@@ -629,7 +652,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
-    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny"], default=None,
+    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny", "fp16"], default=None,
                     help="measure only this workload (no headline line; for profiling)")
     ap.add_argument("--weight", choices=["packed", "plain"], default="packed",
                     help="weight path of the timed step (the other one is measured alongside)")

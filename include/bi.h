@@ -85,28 +85,33 @@ typedef struct {
 
 /*
  * c[m,n] = sum_k a[m,k] * b[k,n]
- *   a: [M,K] bf16, unit stride on K (row-major activations).
- *   b: [K,N] bf16, unit stride on N (row-major weight) or on K (a transposed
- *      view of an [N,K] weight, as torch.nn.functional.linear stores it).
- *   c: [M,N] fp32 or bf16, unit stride on N; written, never read.
+ *   a: [M,K] bf16 or fp16, unit stride on K (row-major activations).
+ *   b: [K,N] of the same type as a, unit stride on N (row-major weight) or on
+ *      K (a transposed view of an [N,K] weight, as torch.nn.functional.linear
+ *      stores it).  Mixed bf16 / fp16 operands return BI_ERR_UNSUPPORTED_DTYPE.
+ *   c: [M,N] fp32, bf16 or fp16, unit stride on N; written, never read.
  *   M, N, K >= 1.  The fp32 accumulator is rounded once to c's dtype (RNE).
+ *   fp16 inputs run the same tile and K order as bf16 inputs (the tensor
+ *   core's f16 kind, one format for both operands).
  */
 bi_status bi_mm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c, bi_stream stream);
 
 /*
  * c[m,n] = (sum_k a[m,k] * b[k,n]) + bias[n]   (alpha = beta = 1)
- *   bias: [N] bf16 or fp32, any stride; added to the fp32 accumulator after
- *   the full K reduction, then one rounding to c's dtype.  Layouts as bi_mm.
+ *   bias: [N] bf16, fp16 or fp32, any stride; added to the fp32 accumulator
+ *   after the full K reduction, then one rounding to c's dtype.  Operand
+ *   types and layouts as bi_mm.
  */
 bi_status bi_addmm(const bi_tensor* bias, const bi_tensor* a, const bi_tensor* b,
                    const bi_tensor* c, bi_stream stream);
 
 /*
  * c[l,m,n] = alpha * sum_k a[l,m,k] * b[l,k,n]   for l in [0, L)
- *   a: [L,M,K] bf16, unit stride on K;  b: [L,K,N] bf16, unit stride on N or
- *   on K (so Q @ K^T passes K^T as a stride view);  c: [L,M,N] fp32 or bf16,
- *   unit stride on N.  The fp32 accumulator is multiplied by alpha (fp32),
- *   then rounded once.  Each l is an independent product.
+ *   a: [L,M,K] bf16 or fp16, unit stride on K;  b: [L,K,N] of the same type,
+ *   unit stride on N or on K (so Q @ K^T passes K^T as a stride view);
+ *   c: [L,M,N] fp32, bf16 or fp16, unit stride on N.  The fp32 accumulator is
+ *   multiplied by alpha (fp32), then rounded once.  Each l is an independent
+ *   product.
  */
 bi_status bi_bmm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c, float alpha,
                  bi_stream stream);
@@ -200,13 +205,14 @@ typedef struct {
   int64_t K, N;     /* logical shape of the packed [K, N] weight */
   int32_t layout;   /* 1: images of a row-major [K,N] weight, 2: of a [N,K] (transposed view) */
   int32_t tile_n;   /* output-tile width the packing was made for (must match the library) */
+  int32_t dtype;    /* element type of the weight: BI_BF16 or BI_F16 */
 } bi_packed_weight;
 
 /* Bytes needed to pack a [K, N] bf16 weight (0 for an empty one). */
 int64_t bi_packed_weight_bytes(int64_t K, int64_t N);
 
 /*
- * Packs b ([K,N] bf16 on the device, unit stride on N or on K, 16-byte aligned
+ * Packs b ([K,N] bf16 or fp16 on the device, unit stride on N or on K, 16-byte aligned
  * base and 16-byte multiple other stride) into dst (device, 16-byte aligned,
  * dst_bytes >= bi_packed_weight_bytes(K, N)); fills *out.  Asynchronous on
  * `stream`; dst must not be used before the packing has run.
@@ -216,9 +222,9 @@ bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_bytes, bi_pa
 
 /*
  * c[m,n] = sum_k a[m,k] * B[k,n] (+ bias[n] when bias is non-NULL with a
- * non-NULL ptr), B given in packed form.  a: [M,K] bf16 as in bi_mm; c: [M,N]
- * fp32 or bf16 as in bi_mm; bias: [N] bf16 or fp32.  Same arithmetic, same
- * bits as bi_mm / bi_addmm on the unpacked weight.
+ * non-NULL ptr), B given in packed form.  a: [M,K] of the packed weight's
+ * type, as in bi_mm; c: [M,N] fp32, bf16 or fp16; bias: [N] bf16, fp16 or
+ * fp32.  Same arithmetic, same bits as bi_mm / bi_addmm on the unpacked weight.
  */
 bi_status bi_addmm_packed(const bi_tensor* bias, const bi_tensor* a, const bi_packed_weight* b,
                           const bi_tensor* c, bi_stream stream);

@@ -41,7 +41,8 @@ class BiTensor(ctypes.Structure):
 
 class BiPackedWeightDesc(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("N", ctypes.c_int64), ("layout", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
+                ("N", ctypes.c_int64), ("layout", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
 
 
 class BiConvPackedWeightDesc(ctypes.Structure):

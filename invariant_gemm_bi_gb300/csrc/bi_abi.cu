@@ -122,7 +122,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzl
   return true;
 }
 
-bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M, int64_t N,
+bool encode_output_map(CUtensorMap* map, void* c, bool f32, bool f16, int64_t L, int64_t M, int64_t N,
                        int64_t ldc, int64_t c_batch) {
   const uint64_t esz = f32 ? 4 : 2;
   const uint64_t row = (uint64_t)ldc * esz;
@@ -134,7 +134,8 @@ bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M
   const cuuint64_t strides[2] = {row, bat};
   const cuuint32_t box[3] = {32, 32, 1};
   std::string why;
-  return encode_tiled(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  return encode_tiled(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                             : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
                       f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, c, 3, dims,
                       strides, box, &why);
 }
@@ -262,13 +263,17 @@ bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor
                       std::string* why, const bi_packed_weight* packed = nullptr) {
   const int nd = batched ? 3 : 2;
   bi_status st;
-  // A packed weight stands in for b as a [K, N] bf16 operand.
+  // A packed weight stands in for b as a [K, N] operand of its element type.
   bi_tensor pb;
   if (packed) {
     memset(&pb, 0, sizeof(pb));
     pb.ptr = packed->ptr;
     pb.ndim = 2;
-    pb.dtype = BI_BF16;
+    pb.dtype = packed->dtype;
+    if (packed->dtype != BI_BF16 && packed->dtype != BI_F16) {
+      *why = "packed weight: unknown element type";
+      return BI_ERR_INVALID_ARG;
+    }
     pb.shape[0] = packed->K;
     pb.shape[1] = packed->N;
     pb.stride[0] = packed->N;
@@ -278,12 +283,15 @@ bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor
   if ((st = check_tensor(a, "a", nd, why)) != BI_OK) return st;
   if ((st = check_tensor(b, "b", nd, why)) != BI_OK) return st;
   if ((st = check_tensor(c, "c", nd, why)) != BI_OK) return st;
-  if (a->dtype != BI_BF16 || b->dtype != BI_BF16) {
-    *why = "a and b must both be bf16";
+  // One input type for both operands: the tensor core's kind::f16 product
+  // takes A and B of the same format (mixing them is refused here, before
+  // anything reaches the GPU).
+  if (!((a->dtype == BI_BF16 && b->dtype == BI_BF16) || (a->dtype == BI_F16 && b->dtype == BI_F16))) {
+    *why = "a and b must both be bf16 or both be fp16";
     return BI_ERR_UNSUPPORTED_DTYPE;
   }
-  if (c->dtype != BI_BF16 && c->dtype != BI_F32) {
-    *why = "c must be bf16 or fp32";
+  if (c->dtype != BI_BF16 && c->dtype != BI_F32 && c->dtype != BI_F16) {
+    *why = "c must be bf16, fp16 or fp32";
     return BI_ERR_UNSUPPORTED_DTYPE;
   }
   const int o = batched ? 1 : 0;  // offset of the matrix dims
@@ -312,10 +320,8 @@ bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor
       bias_kind = 1;
     else if (bias->dtype == BI_F32)
       bias_kind = 2;
-    else {
-      *why = "bias must be bf16 or fp32";
-      return BI_ERR_UNSUPPORTED_DTYPE;
-    }
+    else
+      bias_kind = 3;  // fp16 (check_tensor admits no other code)
     bias_stride = bias->stride[0];
     if (!aligned(bias->ptr, elem_size(bias->dtype))) {
       *why = "bias pointer is not aligned to its element size";
@@ -337,6 +343,8 @@ bi_status matmul_impl(const bi_tensor* bias, const bi_tensor* a, const bi_tensor
   g.bias_stride = bias_stride;
   g.c = c->ptr;
   g.out_f32 = c->dtype == BI_F32;
+  g.out_f16 = c->dtype == BI_F16;
+  g.in_f16 = a->dtype == BI_F16;
   const int cesz = elem_size(c->dtype);
   if (!(N == 1 || c->stride[o + 1] == 1)) {
     *why = "c needs a unit stride on N";
@@ -432,7 +440,7 @@ extern "C" bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_b
   std::string why;
   bi_status st;
   if ((st = check_tensor(b, "b", 2, &why)) != BI_OK) return finish(st, why);
-  if (b->dtype != BI_BF16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "b must be bf16");
+  if (b->dtype != BI_BF16 && b->dtype != BI_F16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "b must be bf16 or fp16");
   if (!out) return finish(BI_ERR_INVALID_ARG, "out: null");
   const int64_t K = b->shape[0], N = b->shape[1];
   if (K == 0 || N == 0) return finish(BI_ERR_INVALID_ARG, "empty weight");
@@ -446,6 +454,7 @@ extern "C" bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_b
   g.L = 1;
   g.K = K;
   g.N = N;
+  g.in_f16 = b->dtype == BI_F16;
   if ((st = normalize_b(b, 0, 1, K, N, false, &g, &why)) != BI_OK) return finish(st, why);
   st = launch_pack(g, dst, (cudaStream_t)stream, &why);
   if (st == BI_OK) {
@@ -455,6 +464,7 @@ extern "C" bi_status bi_pack_weight(const bi_tensor* b, void* dst, int64_t dst_b
     out->N = N;
     out->layout = g.b_mn_major ? 1 : 2;
     out->tile_n = kBN;
+    out->dtype = b->dtype;
   }
   return finish(st, why);
 }
@@ -742,4 +752,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 3; }
+extern "C" int32_t bi_abi_version(void) { return 4; }

@@ -59,8 +59,10 @@ struct GemmParams {
   float alpha;
   int32_t M, N, K, L;
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;
-  int32_t out_f32;    // 1: fp32 output, 0: bf16 output
-  int32_t bias_kind;  // 0: none, 1: bf16, 2: fp32
+  int32_t out_f32;    // 1: fp32 output, 0: 16-bit output
+  int32_t out_f16;    // 16-bit output is fp16 (else bf16)
+  int32_t in_f16;     // A and B are fp16 (else bf16)
+  int32_t bias_kind;  // 0: none, 1: bf16, 2: fp32, 3: fp16
   int32_t vec_store;  // 1: every output row start is 16-byte aligned
   int32_t use_tma_store;
   unsigned int* status_word;

@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv_kernel(const __grid_cons
     o.bias_groups = p.groups;
     o.trans = 0;
     o.tile_rows = kBM;
+    o.out_f16 = 0;
     o.tma_c = p.use_tma_store ? &p.tma_y : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 5) * 2 * kStageOutBytes;
     epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,
@@ -444,7 +445,7 @@ bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* w
                      : 0;
   p.x_vec16 = ((reinterpret_cast<uintptr_t>(cp.x) % 16) == 0 && cp.W % 8 == 0) ? 1 : 0;
   p.w_vec8 = ((reinterpret_cast<uintptr_t>(cp.w) % 8) == 0 && p.Kg % 4 == 0) ? 1 : 0;
-  p.use_tma_store = encode_output_map(&p.tma_y, cp.y, cp.out_f32 != 0, cp.B * cp.groups, p.Cog, p.P,
+  p.use_tma_store = encode_output_map(&p.tma_y, cp.y, cp.out_f32 != 0, false, cp.B * cp.groups, p.Cog, p.P,
                                       p.P, (int64_t)p.Cog * p.P)
                         ? 1
                         : 0;

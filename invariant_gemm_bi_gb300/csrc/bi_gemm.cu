@@ -228,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && crank == 0)
       mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, B_MN, true, kGemmBN, kGemmAcc>(
-          sA, sB, bars, tmem_base, first_tile, p.num_tiles, p.k_blocks, stride, wc);
+          sA, sB, bars, tmem_base, first_tile, p.num_tiles, p.k_blocks, stride, wc, p.in_f16 != 0);
   } else {
     OutDesc o;
     o.c = p.c;
@@ -246,6 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     o.bias_groups = 1;
     o.trans = 0;
     o.tile_rows = kBM;
+    o.out_f16 = p.out_f16;
     o.tma_c = (Lay::STAGING_BYTES > 0 && p.use_tma_store) ? &p.tma_c : nullptr;
     const uint32_t staging = bar0 + Lay::BAR_BYTES + (warp - 2) * 2 * kStageOutBytes;
     epilogue_role<true, kGemmBN, kGemmAcc>(warp & 3, lane, tmem_base, bars, first_tile, p.num_tiles, p.m_tiles,
@@ -313,13 +314,15 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
 // Host side
 // ---------------------------------------------------------------------------
 
+// A 16-bit operand (bf16, or fp16 with f16) as a 3-D tensor map, 128-byte swizzle.
 static bool encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-                      uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1,
+                      uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, bool f16,
                       std::string* why) {
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
   const cuuint32_t box[3] = {b0, b1, 1};
-  return encode_tiled_bf16(map, const_cast<void*>(ptr), 3, dims, strides, box, why);
+  return encode_tiled(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B, const_cast<void*>(ptr), 3, dims, strides, box, why);
 }
 
 // B's tensor map: MN-major as [L][K][N] with 64 x 64 boxes, K-major as
@@ -328,10 +331,10 @@ static bool encode_b(CUtensorMap* map, const GemmProblem& g, uint32_t k_major_ro
   const uint64_t b_row = (uint64_t)g.ldb * 2;
   if (g.b_mn_major) {
     const uint64_t b_bat = g.L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)g.K, 16);
-    return encode_3d(map, g.b, g.N, g.K, g.L, b_row, b_bat, 64, kBK, why);
+    return encode_3d(map, g.b, g.N, g.K, g.L, b_row, b_bat, 64, kBK, g.in_f16 != 0, why);
   }
   const uint64_t b_bat = g.L > 1 ? (uint64_t)g.b_batch * 2 : round_up_u64(b_row * (uint64_t)g.N, 16);
-  return encode_3d(map, g.b, g.K, g.N, g.L, b_row, b_bat, kBK, k_major_rows, why);
+  return encode_3d(map, g.b, g.K, g.N, g.L, b_row, b_bat, kBK, k_major_rows, g.in_f16 != 0, why);
 }
 
 int64_t packed_bytes(int64_t K, int64_t N) {
@@ -403,7 +406,8 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   const bool short_a = M <= kShortARows;
   const uint64_t a_row = (uint64_t)g.lda * 2;
   const uint64_t a_bat = L > 1 ? (uint64_t)g.a_batch * 2 : round_up_u64(a_row * (uint64_t)M, 16);
-  if (!encode_3d(&p.tma_a, g.a, K, M, L, a_row, a_bat, kBK, short_a ? kShortARows : kBM, why))
+  if (!encode_3d(&p.tma_a, g.a, K, M, L, a_row, a_bat, kBK, short_a ? kShortARows : kBM, g.in_f16 != 0,
+                 why))
     return BI_ERR_CUDA;
   if (g.b_packed) {
     // The packed image as [rows][64] bf16 (128-byte rows, no swizzle: the
@@ -413,7 +417,9 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
     const cuuint64_t dims[3] = {64, rows, 1};
     const cuuint64_t strides[2] = {128, rows * 128};
     const cuuint32_t box[3] = {64, kGemmBN / 2 * kBK * 2 / 128, 1};
-    if (rows > INT32_MAX || !encode_tiled(&p.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE,
+    if (rows > INT32_MAX || !encode_tiled(&p.tma_b,
+                                          g.in_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                          CU_TENSOR_MAP_SWIZZLE_NONE,
                                           const_cast<void*>(g.b_packed), 3, dims, strides, box, why))
       return rows > INT32_MAX ? BI_ERR_INVALID_ARG : BI_ERR_CUDA;
   } else if (!encode_b(&p.tma_b, g, kGemmBN / 2, why)) {  // K-major: each CTA's columns
@@ -441,7 +447,10 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   p.out_f32 = g.out_f32;
   p.bias_kind = g.bias_kind;
   p.vec_store = g.vec_store;
-  p.use_tma_store = encode_output_map(&p.tma_c, g.c, g.out_f32 != 0, L, M, N, g.ldc, g.c_batch) ? 1 : 0;
+  p.use_tma_store =
+      encode_output_map(&p.tma_c, g.c, g.out_f32 != 0, g.out_f16 != 0, L, M, N, g.ldc, g.c_batch) ? 1 : 0;
+  p.out_f16 = g.out_f16;
+  p.in_f16 = g.in_f16;
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
 

@@ -46,7 +46,7 @@ inline bool encode_tiled_bf16(CUtensorMap* map, void* ptr, uint32_t rank, const 
 // Tensor map of an output [L][M][N] (row stride ldc, batch stride c_batch,
 // elements) for the epilogue's 32 x 32 tile stores; false when the layout is
 // not TMA-legal (the epilogue then stores directly).
-bool encode_output_map(CUtensorMap* map, void* c, bool f32, int64_t L, int64_t M, int64_t N,
+bool encode_output_map(CUtensorMap* map, void* c, bool f32, bool f16, int64_t L, int64_t M, int64_t N,
                        int64_t ldc, int64_t c_batch);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, slot).
@@ -68,9 +68,11 @@ struct GemmProblem {
   void* c;  // [L][M][N], unit stride on N
   int64_t ldc, c_batch;
   int out_f32;
+  int out_f16;       // 16-bit output is fp16 (else bf16)
+  int in_f16;        // a and b are fp16 (else bf16)
   const void* bias;  // per column n, or null
   int64_t bias_stride;
-  int bias_kind;  // 0 none, 1 bf16, 2 fp32
+  int bias_kind;  // 0 none, 1 bf16, 2 fp32, 3 fp16
   float alpha;
   int64_t L, M, N, K;
   int vec_store;

@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
     o.bias_groups = 1;
     o.trans = 1;
     o.tile_rows = p.tile_rows;
+    o.out_f16 = 0;
     epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,
                   gridDim.x, o, 0u, wc);
   } else {

@@ -30,6 +30,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "bi_common.h"
 #include "bi_ptx.cuh"
@@ -82,8 +83,12 @@ template <int STAGES, int A_BYTES, int B_BYTES, bool B_MN, bool PAIR = false, in
           int ACC = 2>
 __device__ __forceinline__ void mma_role(uint32_t sA, uint32_t sB, const PipeBars& bars,
                                          uint32_t tmem_base, int first_tile, int num_tiles,
-                                         int k_blocks, int stride, const WaitCtl& w) {
-  constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, B_MN);
+                                         int k_blocks, int stride, const WaitCtl& w,
+                                         bool in_f16 = false) {
+  // A and B are both bf16 or both fp16 (one format for both, as kind::f16
+  // requires): fp16 is format code 0 in the A and B fields.
+  const uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, B_MN) &
+                          ~(in_f16 ? ((7u << 7) | (7u << 10)) : 0u);
   constexpr uint16_t kBoth = 3;
   uint32_t it = 0;
   int local = 0;
@@ -158,7 +163,8 @@ struct OutDesc {
   int64_t ldc, c_batch_stride, bias_stride;
   float alpha;
   int32_t M, N;
-  int32_t out_f32, bias_kind, vec_store;
+  int32_t out_f32, bias_kind, vec_store;  // bias_kind: 0 none, 1 bf16, 2 fp32, 3 fp16
+  int32_t out_f16;                        // 16-bit output as fp16 instead of bf16
   int32_t bias_per_row, bias_groups;
   int32_t trans;
   // Tile row r of m block mb is output row mb*tile_rows + r, and only rows
@@ -175,6 +181,10 @@ __device__ __forceinline__ float load_bias(const OutDesc& o, int64_t idx) {
   if (o.bias_kind == 1) {
     const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(o.bias);
     return __bfloat162float(b[idx * o.bias_stride]);
+  }
+  if (o.bias_kind == 3) {
+    const __half* b = reinterpret_cast<const __half*>(o.bias);
+    return __half2float(b[idx * o.bias_stride]);
   }
   return reinterpret_cast<const float*>(o.bias)[idx * o.bias_stride];
 }
@@ -225,7 +235,20 @@ __device__ __forceinline__ void epilogue_math(const OutDesc& o, int j, const Til
   }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// One rounding (RNE) of fp32 values to the 16-bit output type.
+__device__ __forceinline__ uint16_t cvt_out1(const OutDesc& o, float v) {
+  if (o.out_f16) {
+    const __half h = __float2half_rn(v);
+    return *reinterpret_cast<const uint16_t*>(&h);
+  }
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_out2(const OutDesc& o, float lo, float hi) {
+  if (o.out_f16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
@@ -245,10 +268,10 @@ __device__ __forceinline__ void store_32_direct(const OutDesc& o, int l, int m, 
       for (int i = 0; i < 32; ++i)
         if (n0 + i < o.N) dst[(int64_t)(n0 + i) * o.ldc] = f[i];
     } else {
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.c) + base;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(o.c) + base;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (n0 + i < o.N) dst[(int64_t)(n0 + i) * o.ldc] = __float2bfloat16_rn(f[i]);
+        if (n0 + i < o.N) dst[(int64_t)(n0 + i) * o.ldc] = cvt_out1(o, f[i]);
     }
     return;
   }
@@ -266,17 +289,17 @@ __device__ __forceinline__ void store_32_direct(const OutDesc& o, int l, int m, 
         if (n0 + i < o.N) dst[i] = f[i];
     }
   } else {
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.c) + off;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(o.c) + off;
     if (full) {
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        d4[i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
-                           pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+        d4[i] = make_uint4(pack_out2(o, f[8 * i], f[8 * i + 1]), pack_out2(o, f[8 * i + 2], f[8 * i + 3]),
+                           pack_out2(o, f[8 * i + 4], f[8 * i + 5]), pack_out2(o, f[8 * i + 6], f[8 * i + 7]));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (n0 + i < o.N) dst[i] = __float2bfloat16_rn(f[i]);
+        if (n0 + i < o.N) dst[i] = cvt_out1(o, f[i]);
     }
   }
 }
@@ -296,8 +319,8 @@ __device__ __forceinline__ void stage_32(const OutDesc& o, uint32_t sbuf, int la
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
       st_shared_v4(sbuf + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
-                   pack_bf16x2(f[8 * cc], f[8 * cc + 1]), pack_bf16x2(f[8 * cc + 2], f[8 * cc + 3]),
-                   pack_bf16x2(f[8 * cc + 4], f[8 * cc + 5]), pack_bf16x2(f[8 * cc + 6], f[8 * cc + 7]));
+                   pack_out2(o, f[8 * cc], f[8 * cc + 1]), pack_out2(o, f[8 * cc + 2], f[8 * cc + 3]),
+                   pack_out2(o, f[8 * cc + 4], f[8 * cc + 5]), pack_out2(o, f[8 * cc + 6], f[8 * cc + 7]));
   }
 }
 

@@ -10,6 +10,7 @@
 // every lane the same bits (fp32 addition is commutative).  The order depends
 // only on the element index, never on the number of rows or on alignment.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -203,9 +204,13 @@ __global__ void fill_bias_kernel(const GemmProblem g) {
       v = __fadd_rn(v, __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(g.bias)[n * g.bias_stride]));
     else if (g.bias_kind == 2)
       v = __fadd_rn(v, reinterpret_cast<const float*>(g.bias)[n * g.bias_stride]);
+    else if (g.bias_kind == 3)
+      v = __fadd_rn(v, __half2float(reinterpret_cast<const __half*>(g.bias)[n * g.bias_stride]));
     const int64_t off = l * g.c_batch + m * g.ldc + n;
     if (g.out_f32)
       reinterpret_cast<float*>(g.c)[off] = v;
+    else if (g.out_f16)
+      reinterpret_cast<__half*>(g.c)[off] = __float2half_rn(v);
     else
       reinterpret_cast<__nv_bfloat16*>(g.c)[off] = __float2bfloat16_rn(v);
   }

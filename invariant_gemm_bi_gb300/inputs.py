@@ -36,6 +36,13 @@ def normal_bf16(shape, std: float, seed: int, device="cpu") -> torch.Tensor:
     return t.to(torch.bfloat16)
 
 
+def normal_f16(shape, std: float, seed: int, device="cpu") -> torch.Tensor:
+    """N(0, std^2) drawn in fp32, rounded to fp16."""
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.normal_(0.0, std, generator=_gen(seed, device))
+    return t.to(torch.float16)
+
+
 def uniform_bf16(shape, lo: float, hi: float, seed: int, device="cpu") -> torch.Tensor:
     """U(lo, hi) drawn in fp32, rounded to bf16."""
     t = torch.empty(shape, dtype=torch.float32, device=device)
@@ -63,6 +70,17 @@ def tiny_mm(m_max: int = 64, device="cpu"):
     a = normal_bf16((m_max, 256), 1.0, SEED_ACT, device)
     w = normal_bf16((256, 128), 0.02, SEED_WEIGHT, device)
     return a, w
+
+
+LLM_ADDMM_F16_M = (1, 16, 512, 8192)
+
+
+def llm_addmm_f16(m_max: int = 8192, device="cpu", k: int = 4096, n: int = 14336):
+    """The LLM-linear workload with fp16 operands (same distributions and seeds), fp16 output."""
+    x = normal_f16((m_max, k), 1.0, SEED_ACT, device)
+    w = normal_f16((k, n), 0.02, SEED_WEIGHT, device)
+    bias = normal_f16((n,), 0.01, SEED_AUX, device)
+    return x, w, bias
 
 
 def llm_addmm(m_max: int = 8192, device="cpu", k: int = 4096, n: int = 14336):

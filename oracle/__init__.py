@@ -66,10 +66,11 @@ def _load():
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(build())
-            lib.bio_mm.argtypes = [_i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
-                                   _vp, _i64, _dbl, _vp, _i64, _vp, _vp]
+            _int = ctypes.c_int
+            lib.bio_mm.argtypes = [_i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64, _i64,
+                                   _int, _vp, _i64, _dbl, _vp, _i64, _vp, _vp]
             lib.bio_mm.restype = None
-            lib.bio_bmm.argtypes = [_i64, _i64, _i64, _i64, _vp, _i64, _i64, _i64,
+            lib.bio_bmm.argtypes = [_i64, _i64, _i64, _i64, _int, _vp, _i64, _i64, _i64,
                                     _vp, _i64, _i64, _i64, _dbl, _vp, _vp]
             lib.bio_bmm.restype = None
             lib.bio_conv2d.argtypes = [_i64] * 14 + [_vp, _vp, _vp, _vp, _vp]
@@ -90,6 +91,8 @@ def _load():
             lib.bio_sum_seq_f32.restype = ctypes.c_float
             lib.bio_bf16_bits_to_double.argtypes = [ctypes.c_uint16]
             lib.bio_bf16_bits_to_double.restype = _dbl
+            lib.bio_f16_bits_to_double.argtypes = [ctypes.c_uint16]
+            lib.bio_f16_bits_to_double.restype = _dbl
             lib.bio_num_threads.argtypes = []
             lib.bio_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -102,6 +105,13 @@ def _bf16(t: torch.Tensor) -> torch.Tensor:
     return t
 
 
+def _half(t: torch.Tensor) -> int:
+    """1 for an fp16 tensor, 0 for bf16 (the 16-bit types the products take)."""
+    if t.device.type != "cpu" or t.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"oracle expects CPU bfloat16 or float16 tensors, got {t.dtype} on {t.device}")
+    return 1 if t.dtype == torch.float16 else 0
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr() if isinstance(t, torch.Tensor) else t.ctypes.data)
 
@@ -112,7 +122,8 @@ def num_threads() -> int:
 
 def mm(a: torch.Tensor, b: torch.Tensor, bias: torch.Tensor | None = None,
        alpha: float = 1.0, rows=None):
-    """fp64 ``alpha * a @ b (+ bias)`` for bf16 a [M,K], b [K,N] (any strides).
+    """fp64 ``alpha * a @ b (+ bias)`` for bf16 or fp16 a [M,K], b [K,N] of the
+    same type (any strides); bias bf16 or fp16.
 
     Returns ``(c, absum)``: both float64 numpy arrays of shape [R, N], where
     R = M, or len(rows) when only the listed output rows are computed.
@@ -120,7 +131,9 @@ def mm(a: torch.Tensor, b: torch.Tensor, bias: torch.Tensor | None = None,
     the error bound the GPU result is held to.
     """
     lib = _load()
-    _bf16(a), _bf16(b)
+    in_f16 = _half(a)
+    if _half(b) != in_f16:
+        raise TypeError("a and b must have the same dtype")
     M, K = a.shape
     K2, N = b.shape
     if K != K2:
@@ -132,29 +145,30 @@ def mm(a: torch.Tensor, b: torch.Tensor, bias: torch.Tensor | None = None,
         R = int(rows_arr.size)
     c = np.empty((R, N), dtype=np.float64)
     absum = np.empty((R, N), dtype=np.float64)
-    if bias is not None:
-        _bf16(bias)
-    lib.bio_mm(M, N, K, _ptr(a), a.stride(0), a.stride(1), _ptr(b), b.stride(0), b.stride(1),
-               _ptr(bias) if bias is not None else None, bias.stride(0) if bias is not None else 0,
+    bias_f16 = _half(bias) if bias is not None else 0
+    lib.bio_mm(M, N, K, in_f16, _ptr(a), a.stride(0), a.stride(1), _ptr(b), b.stride(0), b.stride(1),
+               bias_f16, _ptr(bias) if bias is not None else None, bias.stride(0) if bias is not None else 0,
                float(alpha), _ptr(rows_arr) if rows_arr is not None else None, R,
                _ptr(c), _ptr(absum))
     return c, absum
 
 
 def bmm(a: torch.Tensor, b: torch.Tensor, alpha: float = 1.0):
-    """fp64 ``alpha * a[l] @ b[l]`` for bf16 a [L,M,K], b [L,K,N] (any strides).
+    """fp64 ``alpha * a[l] @ b[l]`` for bf16 or fp16 a [L,M,K], b [L,K,N] of the same type (any strides).
 
     Returns ``(c, absum)`` float64 arrays of shape [L, M, N].
     """
     lib = _load()
-    _bf16(a), _bf16(b)
+    in_f16 = _half(a)
+    if _half(b) != in_f16:
+        raise TypeError("a and b must have the same dtype")
     L, M, K = a.shape
     L2, K2, N = b.shape
     if L != L2 or K != K2:
         raise ValueError("batch or inner dimensions differ")
     c = np.empty((L, M, N), dtype=np.float64)
     absum = np.empty((L, M, N), dtype=np.float64)
-    lib.bio_bmm(L, M, N, K, _ptr(a), a.stride(0), a.stride(1), a.stride(2),
+    lib.bio_bmm(L, M, N, K, in_f16, _ptr(a), a.stride(0), a.stride(1), a.stride(2),
                 _ptr(b), b.stride(0), b.stride(1), b.stride(2), float(alpha), _ptr(c), _ptr(absum))
     return c, absum
 
@@ -289,3 +303,7 @@ def sum_seq_f32(values) -> float:
 
 def bf16_bits_to_double(bits: int) -> float:
     return float(_load().bio_bf16_bits_to_double(bits & 0xFFFF))
+
+
+def f16_bits_to_double(bits: int) -> float:
+    return float(_load().bio_f16_bits_to_double(bits & 0xFFFF))

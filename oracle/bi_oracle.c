@@ -22,8 +22,8 @@
  *    (one row at a time, "ai-infra handbook: deterministic inference",
  *    section on normalisation and softmax reductions).
  *
- * Inputs are the exact bf16 bit patterns handed to the GPU, widened to
- * double.  Every output element is accumulated on one thread, sequentially
+ * Inputs are the exact bf16 (or, for the products, fp16) bit patterns
+ * handed to the GPU, widened to double.  Every output element is accumulated on one thread, sequentially
  * over ascending reduction index, in double precision.  OpenMP only splits
  * the work over output rows, so results do not depend on the thread count.
  * Rounding to the output type happens once, round-to-nearest-even.
@@ -60,6 +60,36 @@ static void ensure_table(void) {
 
 /* Exposed so the tests can pin it against an independent conversion. */
 double bio_bf16_bits_to_double(uint16_t h) { return bf16_to_double(h); }
+
+/*
+ * IEEE 754 binary16 bits -> double, exactly, from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 is
+ * zero / subnormal (fraction * 2^-24), exponent 31 is infinity / NaN.
+ */
+static double f16_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 31;
+  const int f = h & 1023;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -24);
+  else if (e == 31)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(1024 + f), e - 25);
+  return sign ? -v : v;
+}
+
+static double g_f16_table[65536];
+static int g_f16_ready = 0;
+
+static void ensure_f16_table(void) {
+  if (g_f16_ready) return;
+  for (uint32_t i = 0; i < 65536u; ++i) g_f16_table[i] = f16_to_double((uint16_t)i);
+  g_f16_ready = 1;
+}
+
+double bio_f16_bits_to_double(uint16_t h) { return f16_to_double(h); }
 
 /*
  * double -> bf16 bits with ONE round-to-nearest-even step.
@@ -133,17 +163,17 @@ int bio_num_threads(void) {
  * a time in ascending k; abs_row[n] = sum_k |a b| (+ |bias|) is the scale
  * of the error bound.  acc / acc_abs are scratch rows of length N.
  */
-static void mm_row(int64_t N, int64_t K,
+static void mm_row(int64_t N, int64_t K, const double* tab,
                    const uint16_t* a_row, int64_t sa_k,
                    const uint16_t* b, int64_t sb_k, int64_t sb_n,
-                   const uint16_t* bias, int64_t s_bias, double alpha,
+                   const double* bias_tab, const uint16_t* bias, int64_t s_bias, double alpha,
                    double* c_row, double* abs_row, double* acc, double* acc_abs) {
   for (int64_t n = 0; n < N; ++n) { acc[n] = 0.0; acc_abs[n] = 0.0; }
   for (int64_t k = 0; k < K; ++k) {
-    double av = g_bf16_table[a_row[k * sa_k]];
+    double av = tab[a_row[k * sa_k]];
     const uint16_t* brow = b + k * sb_k;
     for (int64_t n = 0; n < N; ++n) {
-      double p = av * g_bf16_table[brow[n * sb_n]];   /* exact in double */
+      double p = av * tab[brow[n * sb_n]];   /* exact in double */
       acc[n] = acc[n] + p;
       acc_abs[n] = acc_abs[n] + fabs(p);
     }
@@ -152,7 +182,7 @@ static void mm_row(int64_t N, int64_t K,
     double v = alpha * acc[n];
     double va = fabs(alpha) * acc_abs[n];
     if (bias) {
-      double bv = g_bf16_table[bias[n * s_bias]];
+      double bv = bias_tab[bias[n * s_bias]];
       v = v + bv;
       va = va + fabs(bv);
     }
@@ -164,17 +194,21 @@ static void mm_row(int64_t N, int64_t K,
 /*
  * c [R,N] (row-major, fp64) = alpha * a [M,K] @ b [K,N] (+ bias [N]).
  * Strides are in elements; a transposed operand is a stride swap.
+ * in_f16: a and b hold fp16 bits (else bf16); bias_f16: likewise for bias.
  * rows: optional list of n_rows output rows to compute (for sampled checks
  * of very large products); output row i then holds row rows[i].  NULL means
  * all M rows in order.
  */
-void bio_mm(int64_t M, int64_t N, int64_t K,
+void bio_mm(int64_t M, int64_t N, int64_t K, int in_f16,
             const uint16_t* a, int64_t sa_m, int64_t sa_k,
             const uint16_t* b, int64_t sb_k, int64_t sb_n,
-            const uint16_t* bias, int64_t s_bias, double alpha,
+            int bias_f16, const uint16_t* bias, int64_t s_bias, double alpha,
             const int64_t* rows, int64_t n_rows,
             double* c, double* absum) {
   ensure_table();
+  ensure_f16_table();
+  const double* tab = in_f16 ? g_f16_table : g_bf16_table;
+  const double* bias_tab = bias_f16 ? g_f16_table : g_bf16_table;
   int64_t R = rows ? n_rows : M;
   size_t row_bytes = sizeof(double) * (size_t)(N > 0 ? N : 1);
 #pragma omp parallel
@@ -184,7 +218,7 @@ void bio_mm(int64_t M, int64_t N, int64_t K,
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < R; ++i) {
       int64_t m = rows ? rows[i] : i;
-      mm_row(N, K, a + m * sa_m, sa_k, b, sb_k, sb_n, bias, s_bias, alpha,
+      mm_row(N, K, tab, a + m * sa_m, sa_k, b, sb_k, sb_n, bias_tab, bias, s_bias, alpha,
              c + i * N, absum ? absum + i * N : NULL, acc, acc_abs);
     }
     free(acc);
@@ -196,11 +230,13 @@ void bio_mm(int64_t M, int64_t N, int64_t K,
  * Batched product: for l in [0, L): c[l] = alpha * a[l] @ b[l].
  * c is [L, M, N] contiguous fp64.  Each batch element is an independent mm.
  */
-void bio_bmm(int64_t L, int64_t M, int64_t N, int64_t K,
+void bio_bmm(int64_t L, int64_t M, int64_t N, int64_t K, int in_f16,
              const uint16_t* a, int64_t sa_l, int64_t sa_m, int64_t sa_k,
              const uint16_t* b, int64_t sb_l, int64_t sb_k, int64_t sb_n,
              double alpha, double* c, double* absum) {
   ensure_table();
+  ensure_f16_table();
+  const double* tab = in_f16 ? g_f16_table : g_bf16_table;
   size_t row_bytes = sizeof(double) * (size_t)(N > 0 ? N : 1);
 #pragma omp parallel
   {
@@ -210,8 +246,8 @@ void bio_bmm(int64_t L, int64_t M, int64_t N, int64_t K,
     for (int64_t l = 0; l < L; ++l) {
       for (int64_t m = 0; m < M; ++m) {
         int64_t o = (l * M + m) * N;
-        mm_row(N, K, a + l * sa_l + m * sa_m, sa_k, b + l * sb_l, sb_k, sb_n,
-               NULL, 0, alpha, c + o, absum ? absum + o : NULL, acc, acc_abs);
+        mm_row(N, K, tab, a + l * sa_l + m * sa_m, sa_k, b + l * sb_l, sb_k, sb_n,
+               tab, NULL, 0, alpha, c + o, absum ? absum + o : NULL, acc, acc_abs);
       }
     }
     free(acc);

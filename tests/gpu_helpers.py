@@ -6,10 +6,12 @@ Tolerance (per element, from the fp64 oracle value ``ref`` and
 ``absum = |alpha| * sum_k |a_k b_k| (+ |bias|)``):
     fp32 output:  |c - ref| <= 1e-4 * absum
     bf16 output:  |c - ref| <= 1e-4 * absum + 2^-8 * |ref|
+    fp16 output:  |c - ref| <= 1e-4 * absum + 2^-11 * |ref| + 2^-25
 The 1e-4 * absum term covers fp32 accumulation over up to 8192 terms (worst
 case K/16 accumulator roundings of at most 2^-23 relative each: 512 * 1.2e-7
 = 6.1e-5 < 1e-4); 2^-8 |ref| is half a bf16 unit in the last place, the final
-rounding.
+rounding; for fp16 output 2^-11 |ref| is half an fp16 unit in the last place
+and 2^-25 half its subnormal spacing.
 """
 from __future__ import annotations
 
@@ -24,6 +26,8 @@ def check_tolerance(gpu: torch.Tensor, ref: np.ndarray, absum: np.ndarray, what:
     bound = 1e-4 * absum
     if gpu.dtype == torch.bfloat16:
         bound = bound + 2.0 ** -8 * np.abs(ref)
+    elif gpu.dtype == torch.float16:
+        bound = bound + 2.0 ** -11 * np.abs(ref) + 2.0 ** -25
     err = np.abs(g - ref)
     bad = ~(err <= bound)  # NaN counts as a failure
     if bad.any():

@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 3
+    assert lib.bi_abi_version() == 4
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -85,9 +85,13 @@ def test_mm_validation_errors(lib):
     assert _mm(lib, ok_a, _t([48, 32]), ok_c) == binding.BI_ERR_SHAPE_MISMATCH
     # output extent mismatch
     assert _mm(lib, ok_a, ok_b, _t([4, 33], dtype=2)) == binding.BI_ERR_SHAPE_MISMATCH
-    # fp32 / fp16 inputs are not taken
+    # fp32 inputs are not taken, and bf16 / fp16 operands are never mixed (the
+    # tensor core's f16 kind takes one format for both)
     assert _mm(lib, _t([4, 64], dtype=2), ok_b, ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
-    assert _mm(lib, _t([4, 64], dtype=1), _t([64, 32], dtype=1), ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert _mm(lib, _t([4, 64], dtype=1), ok_b, ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert _mm(lib, ok_a, _t([64, 32], dtype=1), ok_c) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert lib.bi_bmm(_r(_t([2, 4, 64], dtype=1)), _r(_t([2, 64, 32])), _r(_t([2, 4, 32], dtype=2)), 1.0,
+                      None) == binding.BI_ERR_UNSUPPORTED_DTYPE
     # wrong rank
     assert _mm(lib, _t([4, 64, 1]), ok_b, ok_c) == binding.BI_ERR_INVALID_ARG
     # null descriptor
@@ -119,6 +123,9 @@ def test_valid_call_without_gpu_reports_no_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     st = _mm(lib, _t([4, 64]), _t([64, 32]), _t([4, 32], dtype=2))
+    assert st == binding.BI_ERR_NO_DEVICE
+    # fp16 operands (both) with fp16 output pass validation the same way
+    st = _mm(lib, _t([4, 64], dtype=1), _t([64, 32], dtype=1), _t([4, 32], dtype=1))
     assert st == binding.BI_ERR_NO_DEVICE
 
 
@@ -161,6 +168,14 @@ def test_packed_weight_size_and_validation(lib):
     assert st == binding.BI_ERR_INVALID_ARG
     # fp32 weight refused
     st = lib.bi_pack_weight(_r(_t([64, 256], dtype=2)), FAKE, 1 << 20, ctypes.byref(desc), None)
+    assert st == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # packed descriptor with an element type other than bf16 / fp16
+    pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 256, 2)
+    st = lib.bi_addmm_packed(None, _r(_t([4, 64])), ctypes.byref(pd), _r(_t([4, 256], dtype=2)), None)
+    assert st == binding.BI_ERR_INVALID_ARG
+    # an fp16 packed weight does not take bf16 activations
+    pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 256, 1)
+    st = lib.bi_addmm_packed(None, _r(_t([4, 64])), ctypes.byref(pd), _r(_t([4, 256], dtype=2)), None)
     assert st == binding.BI_ERR_UNSUPPORTED_DTYPE
     # packed descriptor with a foreign tile width
     pd = binding.BiPackedWeightDesc(FAKE, 1 << 20, 64, 256, 1, 128)

@@ -184,6 +184,59 @@ def test_bmm_against_exact_rationals_and_alpha():
 
 
 # ---------------------------------------------------------------------------
+# fp16 operands
+# ---------------------------------------------------------------------------
+
+def test_f16_decoding_matches_numpy_on_every_bit_pattern():
+    # IEEE binary16 from its definition (oracle) vs numpy's float16 (independent)
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_bits_to_double(int(v)) for v in bits[::7]])
+    exp = ref[::7]
+    nan = np.isnan(exp)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], exp[~nan])
+    for v in (0x0001, 0x03FF, 0x0400, 0x7BFF, 0x7C00, 0xFC00, 0x8000, 0x3C00):
+        assert oracle.f16_bits_to_double(v) == float(np.uint16(v).view(np.float16))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mm_f16_against_exact_rationals(seed):
+    g = torch.Generator().manual_seed(300 + seed)
+    M, N, K = (int(v) for v in torch.randint(1, 6, (3,), generator=g))
+    a = (torch.randn(M, K, generator=g) * 3).to(torch.float16)
+    b = (torch.randn(K, N, generator=g) * 0.5).to(torch.float16)
+    bias = (torch.randn(N, generator=g)).to(torch.float16) if seed % 2 else None
+    alpha = [1.0, 0.0625, 3.0][seed % 3]
+    if seed % 3 == 1:
+        b = b.t().contiguous().t()
+    c, absum = oracle.mm(a, b, bias=bias, alpha=alpha)
+    ex, exabs = _exact_mm(a, b, bias, alpha)
+    for m in range(M):
+        for n in range(N):
+            assert abs(Fraction(c[m, n]) - ex[m][n]) <= Fraction(6, 2 ** 53) * exabs[m][n]
+            assert abs(Fraction(absum[m, n]) - exabs[m][n]) <= Fraction(6, 2 ** 53) * exabs[m][n]
+
+
+def test_mm_and_bmm_f16_small_integers_and_fractions_exact():
+    # fp16 holds 11 significant bits: values like 1023.5 or 2^-14 that bf16
+    # cannot hold must arrive exactly
+    g = torch.Generator().manual_seed(9)
+    a = torch.randint(-1024, 1024, (5, 40), generator=g).to(torch.float16) + 0.5
+    b = torch.randint(-8, 8, (40, 6), generator=g).to(torch.float16)
+    c, _ = oracle.mm(a, b)
+    ref = a.to(torch.float64).numpy() @ b.to(torch.float64).numpy()   # exact: small dyadics
+    assert np.array_equal(c, ref)
+    tiny = torch.full((1, 4), 2.0 ** -14, dtype=torch.float16)
+    c, _ = oracle.mm(tiny, torch.ones(4, 1, dtype=torch.float16))
+    assert c[0, 0] == 4 * 2.0 ** -14
+    cb, _ = oracle.bmm(a[None], b[None], alpha=0.5)
+    assert np.array_equal(cb[0], ref * 0.5)
+    with pytest.raises(TypeError):
+        oracle.mm(a, b.to(torch.bfloat16))
+
+
+# ---------------------------------------------------------------------------
 # Rounding
 # ---------------------------------------------------------------------------
 
