@@ -81,6 +81,12 @@ def _load():
             lib.bio_conv_out_size.restype = _i64
             lib.bio_softmax_rows.argtypes = [_i64, _i64, _vp, _i64, _vp]
             lib.bio_softmax_rows.restype = None
+            lib.bio_rmsnorm_rows.argtypes = [_i64, _i64, _vp, _i64, _vp, _dbl, _vp]
+            lib.bio_rmsnorm_rows.restype = None
+            lib.bio_log_softmax_rows.argtypes = [_i64, _i64, _vp, _i64, _vp]
+            lib.bio_log_softmax_rows.restype = None
+            lib.bio_mean_rows.argtypes = [_i64, _i64, _vp, _i64, _vp, _vp]
+            lib.bio_mean_rows.restype = None
             lib.bio_round_bf16.argtypes = [_vp, _vp, _i64]
             lib.bio_round_bf16.restype = None
             lib.bio_round_f32.argtypes = [_vp, _vp, _i64]
@@ -269,6 +275,49 @@ def softmax_rows(s: torch.Tensor) -> np.ndarray:
     p = np.empty((R, N), dtype=np.float64)
     lib.bio_softmax_rows(R, N, _ptr(s), s.stride(0), _ptr(p))
     return p
+
+
+def _rows_f64(x: torch.Tensor) -> np.ndarray:
+    """A CPU [R, N] tensor of a floating type as a C-contiguous float64 array (exact)."""
+    if x.device.type != "cpu" or x.dim() != 2 or x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+        raise TypeError("expects a CPU fp32 / bf16 / fp16 [R, N] tensor")
+    return np.ascontiguousarray(x.to(torch.float64).numpy())
+
+
+def rmsnorm_rows(x: torch.Tensor, weight: torch.Tensor | None = None, eps: float = 1e-6) -> np.ndarray:
+    """fp64 RMSNorm over the last dim: y = x * (1 / sqrt(mean(x^2) + eps)) * weight."""
+    lib = _load()
+    xd = _rows_f64(x)
+    R, N = xd.shape
+    wd = None
+    if weight is not None:
+        wd = np.ascontiguousarray(weight.to(torch.float64).numpy())
+        if wd.shape != (N,):
+            raise ValueError("weight must have N elements")
+    y = np.empty((R, N), dtype=np.float64)
+    lib.bio_rmsnorm_rows(R, N, _ptr(xd), N, _ptr(wd) if wd is not None else None, float(eps), _ptr(y))
+    return y
+
+
+def log_softmax_rows(s: torch.Tensor) -> np.ndarray:
+    """fp64 log-softmax over the last dim: (s - max) - log(sum exp(s - max))."""
+    lib = _load()
+    sd = _rows_f64(s)
+    R, N = sd.shape
+    y = np.empty((R, N), dtype=np.float64)
+    lib.bio_log_softmax_rows(R, N, _ptr(sd), N, _ptr(y))
+    return y
+
+
+def mean_rows(x: torch.Tensor):
+    """fp64 mean over the last dim; returns (mean [R], mean of |x| [R])."""
+    lib = _load()
+    xd = _rows_f64(x)
+    R, N = xd.shape
+    y = np.empty((R,), dtype=np.float64)
+    ya = np.empty((R,), dtype=np.float64)
+    lib.bio_mean_rows(R, N, _ptr(xd), N, _ptr(y), _ptr(ya))
+    return y, ya
 
 
 def round_bf16(x: np.ndarray) -> torch.Tensor:

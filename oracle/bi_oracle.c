@@ -21,6 +21,11 @@
  *  - softmax over the last dimension: p_j = exp(s_j - max s) / sum_i exp(s_i - max s)
  *    (one row at a time, "ai-infra handbook: deterministic inference",
  *    section on normalisation and softmax reductions).
+ *  - row reductions of "Unmasking the True Culprit" (section "Beyond Matrix
+ *    Multiplication: Other Critical Operations"): RMSNorm
+ *    y_j = x_j * (1 / sqrt(mean_i x_i^2 + eps)) * w_j, log-softmax
+ *    y_j = (x_j - max x) - log(sum_i exp(x_i - max x)), and the mean over the
+ *    last dimension (aten::mean.dim, "Batch-Invariant VLAs").
  *
  * Inputs are the exact bf16 (or, for the products, fp16) bit patterns
  * handed to the GPU, widened to double.  Every output element is accumulated on one thread, sequentially
@@ -370,5 +375,58 @@ void bio_softmax_rows(int64_t R, int64_t N, const float* s, int64_t ss, double* 
       sum = sum + e;
     }
     for (int64_t j = 0; j < N; ++j) p[r * N + j] = p[r * N + j] / sum;
+  }
+}
+
+/* ------------------------------------------------------------------ */
+/* Row reductions over the last dimension (doubles in, doubles out)   */
+/* ------------------------------------------------------------------ */
+
+/*
+ * RMSNorm of each row of x [R, N] (row stride sx): ms = (sum_j x_j^2) / N in
+ * ascending j, r = 1 / sqrt(ms + eps), y_j = (x_j * r) * w_j (w NULL: 1).
+ * y [R, N] contiguous.
+ */
+void bio_rmsnorm_rows(int64_t R, int64_t N, const double* x, int64_t sx, const double* w,
+                      double eps, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    const double* xr = x + r * sx;
+    double ss = 0.0;
+    for (int64_t j = 0; j < N; ++j) ss = ss + xr[j] * xr[j];
+    const double rinv = 1.0 / sqrt(ss / (double)N + eps);
+    for (int64_t j = 0; j < N; ++j) y[r * N + j] = (xr[j] * rinv) * (w ? w[j] : 1.0);
+  }
+}
+
+/*
+ * Log-softmax of each row of s [R, N]: m = max_j s_j,
+ * lse = log(sum_j exp(s_j - m)) in ascending j, y_j = (s_j - m) - lse.
+ */
+void bio_log_softmax_rows(int64_t R, int64_t N, const double* s, int64_t ss, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    const double* sr = s + r * ss;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) m = sr[j] > m ? sr[j] : m;
+    double sum = 0.0;
+    for (int64_t j = 0; j < N; ++j) sum = sum + exp(sr[j] - m);
+    const double lse = log(sum);
+    for (int64_t j = 0; j < N; ++j) y[r * N + j] = (sr[j] - m) - lse;
+  }
+}
+
+/* Mean of each row of x [R, N]: (sum_j x_j in ascending j) / N; absum: sum_j |x_j| / N. */
+void bio_mean_rows(int64_t R, int64_t N, const double* x, int64_t sx, double* y, double* absum) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    const double* xr = x + r * sx;
+    double sum = 0.0, sa = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+      sum = sum + xr[j];
+      sa = sa + fabs(xr[j]);
+    }
+    y[r] = sum / (double)N;
+    if (absum) absum[r] = sa / (double)N;
   }
 }

@@ -237,6 +237,74 @@ def test_mm_and_bmm_f16_small_integers_and_fractions_exact():
 
 
 # ---------------------------------------------------------------------------
+# Row reductions: RMSNorm, log-softmax, mean
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_closed_forms_and_invariances():
+    # constant row 2^k, eps = 0: every output is exactly sign(x) (times w)
+    x = torch.full((2, 12), -8.0)
+    x[1] = 0.25
+    y = oracle.rmsnorm_rows(x, eps=0.0)
+    assert np.array_equal(y, np.sign(x.numpy()).astype(np.float64))
+    # scaling x by a power of two changes nothing when eps = 0
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(5, 37, generator=g)
+    assert np.array_equal(oracle.rmsnorm_rows(x, eps=0.0), oracle.rmsnorm_rows(x * 64, eps=0.0))
+    # with w = 1 and eps = 0 the output's root mean square is 1
+    y = oracle.rmsnorm_rows(x, eps=0.0)
+    assert np.allclose(np.sqrt((y ** 2).mean(1)), 1.0, rtol=1e-14, atol=0)
+    # the weight scales each column: one-hot weight keeps one column
+    w = torch.zeros(37)
+    w[5] = 2.0
+    yw = oracle.rmsnorm_rows(x, w, eps=0.0)
+    assert np.array_equal(yw[:, 5], 2 * y[:, 5]) and not yw[:, :5].any() and not yw[:, 6:].any()
+
+
+def test_rmsnorm_matches_numpy_with_eps():
+    g = torch.Generator().manual_seed(22)
+    x = torch.randn(7, 300, generator=g).to(torch.bfloat16)
+    w = (torch.rand(300, generator=g) + 0.5).to(torch.bfloat16)
+    xd, wd = x.double().numpy(), w.double().numpy()
+    ref = xd * (1.0 / np.sqrt((xd ** 2).mean(1, keepdims=True) + 1e-6)) * wd
+    assert np.allclose(oracle.rmsnorm_rows(x, w, eps=1e-6), ref, rtol=1e-14, atol=0)
+
+
+def test_log_softmax_closed_forms_and_library():
+    # [0, log 3]: softmax is [1/4, 3/4]
+    x = torch.tensor([[0.0, float(np.log(3.0))]], dtype=torch.float64).float()
+    y = oracle.log_softmax_rows(x)
+    xs = x.double().numpy()
+    assert np.allclose(y, xs - np.log(np.exp(xs).sum()), rtol=0, atol=1e-15)
+    # constant row: -log N
+    y = oracle.log_softmax_rows(torch.full((1, 10), 3.5))
+    assert np.allclose(y, -np.log(10.0), rtol=1e-15, atol=0)
+    # exp(y) sums to one; shifting the row by a constant changes nothing
+    g = torch.Generator().manual_seed(23)
+    x = (torch.randn(6, 777, generator=g) * 4).to(torch.bfloat16).float()
+    x[x.abs() < 2.0 ** -12] = 0.0              # so that x + 8 is exact in fp32
+    y = oracle.log_softmax_rows(x)
+    assert np.allclose(np.exp(y).sum(1), 1.0, rtol=1e-13)
+    assert np.allclose(oracle.log_softmax_rows(x + 8.0), y, rtol=0, atol=1e-13)
+    # against scipy's log_softmax (an independent library routine)
+    special = pytest.importorskip("scipy.special")
+    assert np.allclose(y, special.log_softmax(x.double().numpy(), axis=1), rtol=0, atol=1e-12)
+
+
+def test_mean_rows_exact_cases_and_library():
+    # small integers over a power-of-two length: exact
+    g = torch.Generator().manual_seed(24)
+    x = torch.randint(-50, 50, (4, 64), generator=g).float()
+    m, ma = oracle.mean_rows(x)
+    assert np.array_equal(m, x.double().numpy().sum(1) / 64)
+    assert np.array_equal(ma, np.abs(x.double().numpy()).sum(1) / 64)
+    # constant row
+    assert oracle.mean_rows(torch.full((1, 7), -1.5, dtype=torch.bfloat16))[0][0] == -1.5
+    # against numpy's mean
+    x = torch.randn(5, 1001, generator=g).to(torch.float16)
+    assert np.allclose(oracle.mean_rows(x)[0], x.double().numpy().mean(1), rtol=1e-13, atol=1e-16)
+
+
+# ---------------------------------------------------------------------------
 # Rounding
 # ---------------------------------------------------------------------------
 
