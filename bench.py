@@ -292,7 +292,7 @@ def bits_equal(x, y) -> bool:
 
 def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -> dict:
     """The other workloads, once each: ours vs cuBLAS / cuDNN, with row-0 flags.
-    `only` restricts it to one workload (square, conv, attention, tiny)."""
+    `only` restricts it to one workload (square, conv, attention, tiny, fp16, rows)."""
     import torch.nn.functional as F
     from invariant_gemm_bi_gb300 import binding, inputs
     out = {}
@@ -309,6 +309,8 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -
         _tiny(out, binding, inputs, flush_buf, stream, reps)
     if want("fp16"):
         _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
+    if want("rows"):
+        _rows(out, binding, inputs, flush_buf, stream, peaks, reps)
     return out
 
 
@@ -428,6 +430,47 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         del s, p, o
     out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0)}
     del q, k, v
+
+
+def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
+    # the row reductions, HBM-bound: RMSNorm of [R, 4096] bf16 hidden states
+    # with a gain (bf16 out), log-softmax of [R, 128256] fp32 logits (fp32 out),
+    # mean of [R, 4096] bf16 (fp32 out); PyTorch's own kernels alongside
+    hbm = peaks["hbm_gbs"] * 1e9
+
+    def pt(nb, t, t_torch):
+        return {"us": round(t * 1e6, 2), "gbs": round(nb / t / 1e9, 1),
+                "roofline_frac": round(nb / hbm / t, 3), "bound": "hbm", "torch_us": round(t_torch * 1e6, 2)}
+
+    x, w = inputs.rmsnorm_hidden(max(inputs.RMSNORM_ROWS), device="cuda")
+    s = inputs.vocab_logits(max(inputs.LOGITS_ROWS), device="cuda")
+    N, V = x.shape[1], s.shape[1]
+    rms, mean, lsm, r0 = [], [], [], {"rms": {}, "mean": {}, "lsm": {}}
+    for R in inputs.RMSNORM_ROWS:
+        xr = x[:R]
+        y = torch.empty(R, N, dtype=torch.bfloat16, device="cuda")
+        m = torch.empty(R, dtype=torch.float32, device="cuda")
+        t = measure(lambda: binding.bi_rmsnorm_lastdim(xr, w, 1e-6, out=y), flush_buf, stream, reps)
+        tt = measure(lambda: torch.nn.functional.rms_norm(xr, (N,), w, 1e-6), flush_buf, stream, reps)
+        rms.append({"rows": R, **pt(2.0 * (2 * R * N + N), t, tt)})
+        tm = measure(lambda: binding.bi_mean_lastdim(xr, out=m), flush_buf, stream, reps)
+        ttm = measure(lambda: torch.mean(xr, dim=-1, dtype=torch.float32), flush_buf, stream, reps)
+        mean.append({"rows": R, **pt(2.0 * R * N + 4.0 * R, tm, ttm)})
+        r0["rms"][R], r0["mean"][R] = y[:1].clone(), m[:1].clone()
+        del y, m
+    for R in inputs.LOGITS_ROWS:
+        sr = s[:R]
+        y = torch.empty(R, V, dtype=torch.float32, device="cuda")
+        t = measure(lambda: binding.bi_log_softmax_lastdim(sr, out=y), flush_buf, stream, reps)
+        tt = measure(lambda: torch.log_softmax(sr, dim=-1), flush_buf, stream, reps)
+        lsm.append({"rows": R, **pt(8.0 * R * V, t, tt)})
+        r0["lsm"][R] = y[:1].clone()
+        del y
+    eq = {k: all(bits_equal(v[R], v[min(v)]) for R in v) for k, v in r0.items()}
+    out["rmsnorm_hidden_4096"] = {"points": rms, "row0_bit_equal_all_R": eq["rms"]}
+    out["mean_hidden_4096"] = {"points": mean, "row0_bit_equal_all_R": eq["mean"]}
+    out["log_softmax_vocab_128256"] = {"points": lsm, "row0_bit_equal_all_R": eq["lsm"]}
+    del x, w, s
 
 
 def _tiny(out, binding, inputs, flush_buf, stream, reps):
@@ -652,7 +695,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
-    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny", "fp16"], default=None,
+    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny", "fp16", "rows"], default=None,
                     help="measure only this workload (no headline line; for profiling)")
     ap.add_argument("--weight", choices=["packed", "plain"], default="packed",
                     help="weight path of the timed step (the other one is measured alongside)")

@@ -189,6 +189,48 @@ bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_packed_weight
 bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream);
 
 /*
+ * Row reductions over the last dimension -- the normalisation, log-softmax
+ * and mean operations that "Unmasking the True Culprit: Why Temperature=0
+ * Doesn't Mean Deterministic LLM Inference" (section "Beyond Matrix
+ * Multiplication: Other Critical Operations") and "Batch-Invariant VLAs"
+ * (aten::mean.dim) say must reduce each row in one fixed order.  Every row
+ * is reduced by one warp in the order of bi_softmax_lastdim (4-element
+ * groups g, lane g mod 32 adding its elements in ascending index order in
+ * fp32, then a fixed xor butterfly), so a row's result does not depend on
+ * how many rows are reduced with it, on where the row sits in memory or on
+ * the launch.  Each add, multiply, divide and square root is one separately
+ * rounded fp32 operation; the output is rounded once to its type.
+ *
+ * All three: x (or s): [R,N] bf16, fp16 or fp32 with a unit stride on N,
+ * aligned to its element size, N <= 2^24; outputs of any of the three types.
+ * Asynchronous on `stream`; R == 0 (or N == 0 for the first two) launches
+ * nothing.  Shape, layout or type errors are returned before any launch.
+ */
+
+/*
+ * y[r,j] = RN(RN(x[r,j] * inv) * weight[j]),
+ *   inv = RN(1 / RN(sqrt(RN(RN(sum_j x[r,j]^2) / N) + eps))),
+ * the multiply by weight left out when weight is NULL (or weight->ptr is
+ * NULL).  weight: [N] of any of the three types, any stride; y: [R,N], unit
+ * stride on N; eps finite and >= 0 (BI_ERR_INVALID_ARG otherwise).
+ */
+bi_status bi_rmsnorm_lastdim(const bi_tensor* x, const bi_tensor* weight, float eps,
+                             const bi_tensor* y, bi_stream stream);
+
+/*
+ * y[r,j] = RN(RN(s[r,j] - mx) - lse),  mx = max_j s[r,j],
+ *   lse = logf(sum_j expf(RN(s[r,j] - mx))).
+ * y: [R,N], unit stride on N.
+ */
+bi_status bi_log_softmax_lastdim(const bi_tensor* s, const bi_tensor* y, bi_stream stream);
+
+/*
+ * y[r] = RN(RN(sum_j x[r,j]) / N).  y: [R], any stride.  N == 0 with R > 0
+ * is BI_ERR_INVALID_ARG (the mean of an empty row).
+ */
+bi_status bi_mean_lastdim(const bi_tensor* x, const bi_tensor* y, bi_stream stream);
+
+/*
  * Packed weights -- for products whose B operand is a fixed weight streamed
  * from HBM many times (decode-sized M).  Packing stores B as the exact
  * sequence of 128-byte-swizzled 64 x 64 shared-memory tile images the kernel

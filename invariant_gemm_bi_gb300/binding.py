@@ -26,6 +26,7 @@ BI_ERR_TIMEOUT = 6
 BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
+            "bi_rmsnorm_lastdim", "bi_log_softmax_lastdim", "bi_mean_lastdim",
             "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
             "bi_conv_packed_weight_bytes", "bi_conv_pack_weight", "bi_conv2d_patch_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
@@ -110,6 +111,9 @@ def load(path: str | None = None):
                 "bi_conv2d_patch": ([ptr, ptr, ptr, ptr, i32x2, i32x2, i32x2, ctypes.c_int32,
                                      ctypes.c_void_p], st),
                 "bi_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
+                "bi_rmsnorm_lastdim": ([ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
+                "bi_log_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
+                "bi_mean_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_packed_weight_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
                 "bi_pack_weight": ([ptr, ctypes.c_void_p, ctypes.c_int64,
                                     ctypes.POINTER(BiPackedWeightDesc), ctypes.c_void_p], st),
@@ -241,6 +245,42 @@ def bi_softmax_lastdim(s: torch.Tensor, out: torch.Tensor | None = None,
         out = torch.empty(s.shape, dtype=out_dtype, device=s.device)
     ds, dp = _desc(s, "s"), _desc(out, "out")
     _check(lib, "bi_softmax_lastdim", lib.bi_softmax_lastdim(_ref(ds), _ref(dp), _stream(stream)))
+    return out
+
+
+def bi_rmsnorm_lastdim(x: torch.Tensor, weight: torch.Tensor | None = None, eps: float = 1e-6,
+                       out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                       stream=None) -> torch.Tensor:
+    """RMSNorm of each row of a 2-D tensor over its last dimension (output in x's
+    dtype unless out / out_dtype says otherwise)."""
+    lib = load()
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    dx, dw, dy = _desc(x, "x"), _desc(weight, "weight"), _desc(out, "out")
+    _check(lib, "bi_rmsnorm_lastdim",
+           lib.bi_rmsnorm_lastdim(_ref(dx), _ref(dw), ctypes.c_float(eps), _ref(dy), _stream(stream)))
+    return out
+
+
+def bi_log_softmax_lastdim(s: torch.Tensor, out: torch.Tensor | None = None,
+                           out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """Row log-softmax of a 2-D tensor over its last dimension."""
+    lib = load()
+    if out is None:
+        out = torch.empty(s.shape, dtype=out_dtype, device=s.device)
+    ds, dy = _desc(s, "s"), _desc(out, "out")
+    _check(lib, "bi_log_softmax_lastdim", lib.bi_log_softmax_lastdim(_ref(ds), _ref(dy), _stream(stream)))
+    return out
+
+
+def bi_mean_lastdim(x: torch.Tensor, out: torch.Tensor | None = None,
+                    out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """Mean of each row of a 2-D tensor over its last dimension: a [R] result."""
+    lib = load()
+    if out is None:
+        out = torch.empty((x.shape[0],), dtype=out_dtype, device=x.device)
+    dx, dy = _desc(x, "x"), _desc(out, "out")
+    _check(lib, "bi_mean_lastdim", lib.bi_mean_lastdim(_ref(dx), _ref(dy), _stream(stream)))
     return out
 
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -676,6 +677,113 @@ extern "C" bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_pa
   return finish(st, why);
 }
 
+// ---------------------------------------------------------------------------
+// Row reductions: RMSNorm, log-softmax, mean
+// ---------------------------------------------------------------------------
+namespace {
+
+int kind_of(int dtype) { return dtype == BI_F32 ? 2 : (dtype == BI_F16 ? 1 : 0); }
+
+// x: [R, N] of any floating type with a unit stride on N; y: [R, N] (or [R]
+// for the mean) of any floating type.  Fills the shared fields of rp.
+bi_status check_rows(const bi_tensor* x, const bi_tensor* y, bool y_is_row_vector, RowParams* rp,
+                     std::string* why) {
+  bi_status st;
+  if ((st = check_tensor(x, "x", 2, why)) != BI_OK) return st;
+  if ((st = check_tensor(y, "y", y_is_row_vector ? 1 : 2, why)) != BI_OK) return st;
+  const int64_t R = x->shape[0], N = x->shape[1];
+  if (y_is_row_vector ? (y->shape[0] != R) : (y->shape[0] != R || y->shape[1] != N)) {
+    *why = y_is_row_vector ? "y must be [R]" : "y must have x's shape";
+    return BI_ERR_SHAPE_MISMATCH;
+  }
+  if (N > 1 && x->stride[1] != 1) {
+    *why = "x needs a unit stride on its last dimension";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  if (!y_is_row_vector && N > 1 && y->stride[1] != 1) {
+    *why = "y needs a unit stride on its last dimension";
+    return BI_ERR_UNSUPPORTED_LAYOUT;
+  }
+  if (N > (1 << 24)) {
+    *why = "rows longer than 2^24 elements are not supported (N must be exact in fp32)";
+    return BI_ERR_INVALID_ARG;
+  }
+  rp->x = x->ptr;
+  rp->y = y->ptr;
+  rp->R = R;
+  rp->N = N;
+  rp->ld_x = R > 1 ? x->stride[0] : N;
+  rp->ld_y = y_is_row_vector ? y->stride[0] : (R > 1 ? y->stride[0] : N);
+  rp->x_kind = kind_of(x->dtype);
+  rp->y_kind = kind_of(y->dtype);
+  rp->x_esz = elem_size(x->dtype);
+  rp->y_esz = elem_size(y->dtype);
+  if (R > 0 && N > 0) {
+    if (!x->ptr || !y->ptr) {
+      *why = "null data pointer";
+      return BI_ERR_INVALID_ARG;
+    }
+    if (!aligned(x->ptr, rp->x_esz) || !aligned(y->ptr, rp->y_esz)) {
+      *why = "pointers must be aligned to their element size";
+      return BI_ERR_UNSUPPORTED_LAYOUT;
+    }
+  }
+  return BI_OK;
+}
+
+bi_status run_rows(int op, const RowParams& rp, bi_stream stream) {
+  std::string why;
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, &why);
+  if (st == BI_OK) st = launch_row_reduction(op, rp, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
+}  // namespace
+
+extern "C" bi_status bi_rmsnorm_lastdim(const bi_tensor* x, const bi_tensor* weight, float eps,
+                                        const bi_tensor* y, bi_stream stream) {
+  std::string why;
+  RowParams rp;
+  memset(&rp, 0, sizeof(rp));
+  bi_status st = check_rows(x, y, false, &rp, &why);
+  if (st != BI_OK) return finish(st, why);
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return finish(BI_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  rp.eps = eps;
+  if (weight && weight->ptr) {
+    if ((st = check_tensor(weight, "weight", 1, &why)) != BI_OK) return finish(st, why);
+    if (weight->shape[0] != rp.N) return finish(BI_ERR_SHAPE_MISMATCH, "weight must have N elements");
+    if (!aligned(weight->ptr, elem_size(weight->dtype)))
+      return finish(BI_ERR_UNSUPPORTED_LAYOUT, "weight pointer is not aligned to its element size");
+    rp.w = weight->ptr;
+    rp.w_kind = kind_of(weight->dtype);
+    rp.w_stride = weight->stride[0];
+  }
+  if (rp.R == 0 || rp.N == 0) return finish(BI_OK, why);
+  return run_rows(kRowRmsNorm, rp, stream);
+}
+
+extern "C" bi_status bi_log_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
+  std::string why;
+  RowParams rp;
+  memset(&rp, 0, sizeof(rp));
+  bi_status st = check_rows(s, p, false, &rp, &why);
+  if (st != BI_OK) return finish(st, why);
+  if (rp.R == 0 || rp.N == 0) return finish(BI_OK, why);
+  return run_rows(kRowLogSoftmax, rp, stream);
+}
+
+extern "C" bi_status bi_mean_lastdim(const bi_tensor* x, const bi_tensor* y, bi_stream stream) {
+  std::string why;
+  RowParams rp;
+  memset(&rp, 0, sizeof(rp));
+  bi_status st = check_rows(x, y, true, &rp, &why);
+  if (st != BI_OK) return finish(st, why);
+  if (rp.R == 0) return finish(BI_OK, why);
+  if (rp.N == 0) return finish(BI_ERR_INVALID_ARG, "the mean of an empty row is undefined");
+  return run_rows(kRowMean, rp, stream);
+}
+
 extern "C" bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
   std::string why;
   bi_status st;
@@ -752,4 +860,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 4; }
+extern "C" int32_t bi_abi_version(void) { return 5; }

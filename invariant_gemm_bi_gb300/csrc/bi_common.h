@@ -107,6 +107,18 @@ struct PatchParams {
   uint64_t wait_limit_ns;
 };
 
+// Row reductions over the last dimension (see bi_rows.cu).
+enum : int { kRowRmsNorm = 0, kRowLogSoftmax = 1, kRowMean = 2 };
+struct RowParams {
+  const void* x;  // [R][N], row stride ld_x elements, unit column stride
+  void* y;        // [R][N] (row stride ld_y), or for the mean [R] (stride ld_y)
+  const void* w;  // RMSNorm weight [N] (stride w_stride), or null
+  int64_t R, N, ld_x, ld_y, w_stride;
+  int32_t x_kind, y_kind, w_kind;  // 0 bf16, 1 fp16, 2 fp32
+  int32_t x_esz, y_esz;            // element sizes in bytes
+  float eps;
+};
+
 struct SoftmaxParams {
   const float* s;
   void* p;

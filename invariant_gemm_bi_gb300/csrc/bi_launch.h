@@ -115,6 +115,9 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
 
 bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::string* why);
 
+// op: kRowRmsNorm, kRowLogSoftmax or kRowMean.
+bi_status launch_row_reduction(int op, const RowParams& rp, cudaStream_t stream, std::string* why);
+
 bi_status launch_fill_bias(const GemmProblem& g, cudaStream_t stream, std::string* why);
 
 bi_status launch_debug_wait(uint64_t limit_ns, cudaStream_t stream, std::string* why);

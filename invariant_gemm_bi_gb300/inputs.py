@@ -1,9 +1,11 @@
-"""Seeded synthetic inputs for the five contraction workloads.
+"""Seeded synthetic inputs for the five contraction workloads and the row
+reductions.
 
 This module draws random numbers and nothing else: it holds none of the
 contractions' arithmetic, so both the CUDA path and the CPU oracle can take
 their inputs from it.  Every tensor is drawn in fp32 from a seeded
-``torch.Generator`` and rounded once to bf16 (round-to-nearest-even).
+``torch.Generator`` and rounded once to bf16 or fp16 (round-to-nearest-even),
+except the fp32 logits, which are kept as drawn.
 
 Seed scheme: the activation-like operand (A, x, images, Q) uses seed 0, the
 weight-like operand (W, K) seed 1, bias / V seed 2.  Sweeps over M (or B)
@@ -48,6 +50,13 @@ def uniform_bf16(shape, lo: float, hi: float, seed: int, device="cpu") -> torch.
     t = torch.empty(shape, dtype=torch.float32, device=device)
     t.uniform_(lo, hi, generator=_gen(seed, device))
     return t.to(torch.bfloat16)
+
+
+def normal_f32(shape, std: float, seed: int, device="cpu") -> torch.Tensor:
+    """N(0, std^2) drawn in fp32 (no rounding)."""
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.normal_(0.0, std, generator=_gen(seed, device))
+    return t
 
 
 def small_int_bf16(shape, lo: int, hi: int, seed: int, device="cpu") -> torch.Tensor:
@@ -112,3 +121,21 @@ def square_mm(m_max: int = 16384, device="cpu", n: int = 8192):
     a = normal_bf16((m_max, n), 1.0, SEED_ACT, device)
     w = normal_bf16((n, n), 0.01, SEED_WEIGHT, device)
     return a, w
+
+
+# -- row reductions over the last dimension -----------------------------------
+
+RMSNORM_ROWS = (1, 8, 64, 512, 8192)
+LOGITS_ROWS = (1, 8, 64)
+
+
+def rmsnorm_hidden(rows: int = 8192, device="cpu", n: int = 4096):
+    """Hidden states x [rows, 4096] ~N(0,1) bf16 and an RMSNorm gain [4096] ~U(0.5,1.5) bf16."""
+    x = normal_bf16((rows, n), 1.0, SEED_ACT, device)
+    w = uniform_bf16((n,), 0.5, 1.5, SEED_WEIGHT, device)
+    return x, w
+
+
+def vocab_logits(rows: int = 64, device="cpu", n: int = 128256):
+    """Next-token logits [rows, 128256] ~N(0, 3^2) in fp32 (a Llama-3-sized vocabulary)."""
+    return normal_f32((rows, n), 3.0, SEED_ACT, device)

@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 4
+    assert lib.bi_abi_version() == 5
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -227,3 +227,42 @@ def test_conv_packed_weight_size_and_validation(lib):
     assert conv(x, pw, _t([2, 1152, 16, 16], dtype=1)) == binding.BI_ERR_UNSUPPORTED_DTYPE
     # nothing to compute: OK before any CUDA call
     assert conv(_t([0, 3, 224, 224]), pw, _t([0, 1152, 16, 16])) == binding.BI_OK
+
+
+def test_row_reduction_validation(lib):
+    import ctypes as ct
+    x, y = _t([4, 100]), _t([4, 100])
+    eps = ct.c_float(1e-6)
+    # shapes
+    assert lib.bi_rmsnorm_lastdim(_r(x), None, eps, _r(_t([4, 99])), None) == binding.BI_ERR_SHAPE_MISMATCH
+    assert lib.bi_rmsnorm_lastdim(_r(x), _r(_t([99])), eps, _r(y), None) == binding.BI_ERR_SHAPE_MISMATCH
+    assert lib.bi_log_softmax_lastdim(_r(x), _r(_t([3, 100])), None) == binding.BI_ERR_SHAPE_MISMATCH
+    assert lib.bi_mean_lastdim(_r(x), _r(_t([5])), None) == binding.BI_ERR_SHAPE_MISMATCH
+    assert lib.bi_mean_lastdim(_r(x), _r(_t([4, 1])), None) == binding.BI_ERR_INVALID_ARG  # rank
+    # layouts: no unit stride on the reduced dimension, misaligned element
+    assert lib.bi_log_softmax_lastdim(_r(_t([4, 100], [1, 4])), _r(y), None) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert lib.bi_rmsnorm_lastdim(_r(x), None, eps, _r(_t([4, 100], [1, 4])), None) == \
+        binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert lib.bi_mean_lastdim(_r(_t([4, 100], dtype=2, ptr=FAKE + 2)), _r(_t([4])), None) == \
+        binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # eps must be finite and >= 0
+    for bad in (-1.0, float("nan"), float("inf")):
+        assert lib.bi_rmsnorm_lastdim(_r(x), None, ct.c_float(bad), _r(y), None) == binding.BI_ERR_INVALID_ARG
+    # rows longer than 2^24 are refused; an empty row has no mean
+    assert lib.bi_mean_lastdim(_r(_t([1, (1 << 24) + 1])), _r(_t([1])), None) == binding.BI_ERR_INVALID_ARG
+    assert lib.bi_mean_lastdim(_r(_t([3, 0])), _r(_t([3])), None) == binding.BI_ERR_INVALID_ARG
+    # empty problems are no-ops before any CUDA call
+    assert lib.bi_rmsnorm_lastdim(_r(_t([0, 8])), None, eps, _r(_t([0, 8])), None) == binding.BI_OK
+    assert lib.bi_log_softmax_lastdim(_r(_t([5, 0])), _r(_t([5, 0])), None) == binding.BI_OK
+    assert lib.bi_mean_lastdim(_r(_t([0, 8])), _r(_t([0])), None) == binding.BI_OK
+    # a valid call of every input / output type combination gets as far as the device
+    import torch
+    if not torch.cuda.is_available():
+        for dx in (0, 1, 2):
+            for dy in (0, 1, 2):
+                assert lib.bi_rmsnorm_lastdim(_r(_t([4, 100], dtype=dx)), _r(_t([100], dtype=dy)), eps,
+                                              _r(_t([4, 100], dtype=dy)), None) == binding.BI_ERR_NO_DEVICE
+                assert lib.bi_log_softmax_lastdim(_r(_t([4, 100], dtype=dx)), _r(_t([4, 100], dtype=dy)),
+                                                  None) == binding.BI_ERR_NO_DEVICE
+                assert lib.bi_mean_lastdim(_r(_t([4, 100], dtype=dx)), _r(_t([4], dtype=dy)),
+                                           None) == binding.BI_ERR_NO_DEVICE
