@@ -22,6 +22,10 @@ Operation definitions followed (page title, section):
   * softmax     -- the last-dimension softmax of the attention scores, one row
     at a time ("ai-infra handbook: deterministic inference", section on
     normalisation / softmax reductions).
+  * attention   -- o = softmax(scale * q @ k^T) @ v per head over the whole
+    key range ("ai-infra handbook: deterministic inference", section on fixed
+    splitting: attention's key/value range split by a fixed length or not at
+    all, its result independent of how queries are chunked).
 
 Parity pins for every function are in ``tests/test_oracle_pins.py``.
 """
@@ -87,6 +91,8 @@ def _load():
             lib.bio_log_softmax_rows.restype = None
             lib.bio_mean_rows.argtypes = [_i64, _i64, _vp, _i64, _vp, _vp]
             lib.bio_mean_rows.restype = None
+            lib.bio_attention.argtypes = [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _dbl, _vp, _vp, _vp]
+            lib.bio_attention.restype = None
             lib.bio_round_bf16.argtypes = [_vp, _vp, _i64]
             lib.bio_round_bf16.restype = None
             lib.bio_round_f32.argtypes = [_vp, _vp, _i64]
@@ -318,6 +324,26 @@ def mean_rows(x: torch.Tensor):
     ya = np.empty((R,), dtype=np.float64)
     lib.bio_mean_rows(R, N, _ptr(xd), N, _ptr(y), _ptr(ya))
     return y, ya
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float):
+    """fp64 attention per head: q [L, Tq, D], k / v [L, Tk, D] (bf16, fp16 or
+    fp32 CPU tensors, any strides).  Returns (o [L, Tq, D], absum [L, Tq, D]
+    = sum_j p_j |v_jd|, smax [L, Tq] = |scale| max_j sum_d |q_d k_jd|)."""
+    lib = _load()
+    for t in (q, k, v):
+        if t.device.type != "cpu" or t.dim() != 3 or t.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+            raise TypeError("attention expects CPU fp32 / bf16 / fp16 [L, T, D] tensors")
+    L, Tq, D = q.shape
+    Tk = k.shape[1]
+    if k.shape != (L, Tk, D) or v.shape != (L, Tk, D):
+        raise ValueError("k and v must be [L, Tk, D] with q's L and D")
+    qd, kd, vd = (np.ascontiguousarray(t.to(torch.float64).numpy()) for t in (q, k, v))
+    o = np.empty((L, Tq, D), dtype=np.float64)
+    ab = np.empty((L, Tq, D), dtype=np.float64)
+    sm = np.empty((L, Tq), dtype=np.float64)
+    lib.bio_attention(L, Tq, Tk, D, _ptr(qd), _ptr(kd), _ptr(vd), float(scale), _ptr(o), _ptr(ab), _ptr(sm))
+    return o, ab, sm
 
 
 def round_bf16(x: np.ndarray) -> torch.Tensor:

@@ -26,6 +26,11 @@
  *    y_j = x_j * (1 / sqrt(mean_i x_i^2 + eps)) * w_j, log-softmax
  *    y_j = (x_j - max x) - log(sum_i exp(x_i - max x)), and the mean over the
  *    last dimension (aten::mean.dim, "Batch-Invariant VLAs").
+ *  - attention: o[i,:] = sum_j softmax_j(scale * q_i . k_j) v[j,:] per query
+ *    row i of each head, the whole key range at once ("ai-infra handbook:
+ *    deterministic inference", section on fixed splitting, attention: the
+ *    key/value range is split by a fixed length or not at all, and the
+ *    result must not depend on how the queries are chunked).
  *
  * Inputs are the exact bf16 (or, for the products, fp16) bit patterns
  * handed to the GPU, widened to double.  Every output element is accumulated on one thread, sequentially
@@ -428,5 +433,59 @@ void bio_mean_rows(int64_t R, int64_t N, const double* x, int64_t sx, double* y,
     }
     y[r] = sum / (double)N;
     if (absum) absum[r] = sa / (double)N;
+  }
+}
+
+/* ------------------------------------------------------------------ */
+/* Attention (doubles in, doubles out)                                */
+/* ------------------------------------------------------------------ */
+
+/*
+ * q [L, Tq, D], k and v [L, Tk, D], all contiguous.  Per head l and query
+ * row i:
+ *   s_j   = scale * sum_d q[i,d] * k[j,d]       (ascending d)
+ *   m     = max_j s_j
+ *   e_j   = exp(s_j - m),  den = sum_j e_j      (ascending j)
+ *   o[i,d]     = (sum_j e_j * v[j,d]) / den     (ascending j)
+ *   absum[i,d] = (sum_j e_j * |v[j,d]|) / den   (the size of the terms)
+ *   smax[i]    = scale * max_j sum_d |q[i,d] * k[j,d]|
+ * absum and smax feed the tests' error bounds; either may be NULL.
+ */
+void bio_attention(int64_t L, int64_t Tq, int64_t Tk, int64_t D, const double* q, const double* k,
+                   const double* v, double scale, double* o, double* absum, double* smax) {
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t row = 0; row < L * Tq; ++row) {
+    const int64_t l = row / Tq;
+    const double* qi = q + row * D;
+    const double* kl = k + l * Tk * D;
+    const double* vl = v + l * Tk * D;
+    double* e = (double*)malloc((size_t)Tk * sizeof(double));
+    double m = -INFINITY, sm = 0.0;
+    for (int64_t j = 0; j < Tk; ++j) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t d = 0; d < D; ++d) {
+        acc = acc + qi[d] * kl[j * D + d];
+        aacc = aacc + fabs(qi[d] * kl[j * D + d]);
+      }
+      e[j] = scale * acc;
+      if (e[j] > m) m = e[j];
+      if (fabs(scale) * aacc > sm) sm = fabs(scale) * aacc;
+    }
+    double den = 0.0;
+    for (int64_t j = 0; j < Tk; ++j) {
+      e[j] = exp(e[j] - m);
+      den = den + e[j];
+    }
+    for (int64_t d = 0; d < D; ++d) {
+      double num = 0.0, anum = 0.0;
+      for (int64_t j = 0; j < Tk; ++j) {
+        num = num + e[j] * vl[j * D + d];
+        anum = anum + e[j] * fabs(vl[j * D + d]);
+      }
+      o[row * D + d] = num / den;
+      if (absum) absum[row * D + d] = anum / den;
+    }
+    if (smax) smax[row] = sm;
+    free(e);
   }
 }

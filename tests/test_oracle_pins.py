@@ -304,6 +304,72 @@ def test_mean_rows_exact_cases_and_library():
     assert np.allclose(oracle.mean_rows(x)[0], x.double().numpy().mean(1), rtol=1e-13, atol=1e-16)
 
 
+def _qkv(L, Tq, Tk, D, seed, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    return tuple(torch.randn(shape, generator=g).to(dtype) for shape in ((L, Tq, D), (L, Tk, D), (L, Tk, D)))
+
+
+def test_attention_special_cases():
+    q, k, v = _qkv(2, 5, 7, 16, 31)
+    # one key: every query row returns that key's value row, exactly
+    o, ab, _ = oracle.attention(q, k[:, :1], v[:, :1], 0.25)
+    assert np.array_equal(o, np.broadcast_to(v[:, :1].double().numpy(), o.shape))
+    # identical keys: uniform weights, the mean of the value rows
+    ksame = k[:, :1].expand(2, 7, 16).contiguous()
+    o, _, _ = oracle.attention(q, ksame, v, 0.25)
+    assert np.allclose(o, np.broadcast_to(v.double().numpy().mean(1, keepdims=True), o.shape), rtol=1e-14, atol=1e-15)
+    # all-ones values: every output is 1
+    o, _, _ = oracle.attention(q, k, torch.ones_like(v), 0.25)
+    assert np.allclose(o, 1.0, rtol=1e-15, atol=0)
+    # one dominant key (score 900 above the rest): its value row, exactly
+    qd = torch.zeros(1, 3, 8)
+    qd[0, :, 0] = 30.0
+    kd = torch.zeros(1, 6, 8)
+    kd[0, 4, 0] = 30.0
+    vd = torch.randn(1, 6, 8, generator=torch.Generator().manual_seed(32))
+    o, _, _ = oracle.attention(qd, kd, vd, 1.0)
+    assert np.array_equal(o[0], np.broadcast_to(vd[0, 4].double().numpy(), (3, 8)))
+    # two keys with a known score gap: weights 1/(1+e^-g) and e^-g/(1+e^-g)
+    q2 = torch.tensor([[[1.0, 0.0]]])
+    k2 = torch.tensor([[[2.0, 0.0], [0.5, 0.0]]])
+    v2 = torch.tensor([[[1.0, 0.0], [0.0, 1.0]]])
+    o, _, sm = oracle.attention(q2, k2, v2, 0.5)
+    g = 0.5 * (2.0 - 0.5)
+    assert np.allclose(o[0, 0], [1 / (1 + np.exp(-g)), np.exp(-g) / (1 + np.exp(-g))], rtol=1e-15, atol=0)
+    assert sm[0, 0] == 1.0  # 0.5 * max(|1*2|, |1*0.5|)
+
+
+def test_attention_invariances_and_library():
+    q, k, v = _qkv(3, 9, 40, 24, 33)
+    o, ab, sm = oracle.attention(q, k, v, 0.2)
+    # permuting keys and values together changes nothing
+    perm = torch.randperm(40, generator=torch.Generator().manual_seed(34))
+    op, _, _ = oracle.attention(q, k[:, perm], v[:, perm], 0.2)
+    assert np.allclose(op, o, rtol=1e-13, atol=1e-15)
+    # adding one vector u to every key shifts all scores of a row by q.u: no change
+    u = torch.randn(24, generator=torch.Generator().manual_seed(35)).to(torch.bfloat16).float()
+    os_, _, _ = oracle.attention(q.float(), k.float() + u, v, 0.2)
+    assert np.allclose(os_, o, rtol=1e-12, atol=1e-14)
+    # scale 2 equals doubling q (exact in binary floating point)
+    o2, _, _ = oracle.attention(q, k, v, 0.4)
+    o2b, _, _ = oracle.attention(q.float() * 2, k, v, 0.2)
+    assert np.array_equal(o2, o2b)
+    # each head and each query row stands alone
+    o1, _, _ = oracle.attention(q[1:2, 4:5], k[1:2], v[1:2], 0.2)
+    assert np.array_equal(o1[0, 0], o[1, 4])
+    # absum bounds |o|, equals o for non-negative values; smax by brute force
+    assert np.all(ab >= np.abs(o) - 1e-15)
+    vp = v.abs()
+    op_, abp, _ = oracle.attention(q, k, vp, 0.2)
+    assert np.allclose(abp, op_, rtol=1e-15, atol=0)
+    qd, kd = q.double().numpy(), k.double().numpy()
+    assert np.allclose(sm, 0.2 * np.abs(qd[:, :, None, :] * kd[:, None, :, :]).sum(-1).max(-1), rtol=1e-14)
+    # against scipy's softmax and numpy's matrix products (independent routines)
+    special = pytest.importorskip("scipy.special")
+    ref = special.softmax(0.2 * qd @ kd.transpose(0, 2, 1), axis=-1) @ v.double().numpy()
+    assert np.allclose(o, ref, rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------------------
 # Rounding
 # ---------------------------------------------------------------------------
