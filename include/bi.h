@@ -189,6 +189,31 @@ bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_packed_weight
 bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream);
 
 /*
+ * Fused attention, per head l and query row i:
+ *   o[l,i,:] = sum_j softmax_j(scale * q[l,i,:] . k[l,j,:]) v[l,j,:]
+ * in one kernel, the scores and probabilities never written to memory
+ * ("ai-infra handbook: deterministic inference", section on fixed splitting:
+ * attention's key range is not split by load -- here not split at all -- and
+ * a query row's result does not depend on how queries are chunked).  Per
+ * query row: key blocks of 128 in ascending order; scores from a fixed
+ * sequence of tensor-core steps over the head dimension (fp32); t = RN(s * c)
+ * with c = RN(scale * log2 e); a running maximum m, replaced only when a block
+ * raises it by more than 8; p = 2^(t - m) (the SFU's approximation);
+ * l = RN(l * 2^(m_old - m_new)) + sum p (keys ascending); O accumulated in
+ * fp32 from bf16(p) v in key order (rescaled with m); o = RN(O * RN(1/l)),
+ * rounded once to o's type.  None of it depends on L, Tq, the tile a row
+ * falls in or the SM count: a head alone gives the bits it gives in any
+ * batch, and a query row the bits it gives among any other query rows.
+ *   q: [L,Tq,256], k and v: [L,Tk,256], bf16, unit stride on the head
+ *   dimension, 16-byte aligned bases, row and batch strides multiples of 16
+ *   bytes;  o: [L,Tq,256] fp32 or bf16 (same layout rules);  scale finite.
+ *   Tk >= 1 (BI_ERR_INVALID_ARG otherwise); L == 0 or Tq == 0 launches
+ *   nothing.  Non-causal, no mask; head dimension 256 only.
+ */
+bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                       const bi_tensor* o, bi_stream stream);
+
+/*
  * Row reductions over the last dimension -- the normalisation, log-softmax
  * and mean operations that "Unmasking the True Culprit: Why Temperature=0
  * Doesn't Mean Deterministic LLM Inference" (section "Beyond Matrix

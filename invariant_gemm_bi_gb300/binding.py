@@ -26,7 +26,7 @@ BI_ERR_TIMEOUT = 6
 BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
-            "bi_rmsnorm_lastdim", "bi_log_softmax_lastdim", "bi_mean_lastdim",
+            "bi_rmsnorm_lastdim", "bi_log_softmax_lastdim", "bi_mean_lastdim", "bi_attention",
             "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
             "bi_conv_packed_weight_bytes", "bi_conv_pack_weight", "bi_conv2d_patch_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
@@ -114,6 +114,7 @@ def load(path: str | None = None):
                 "bi_rmsnorm_lastdim": ([ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
                 "bi_log_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_mean_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
+                "bi_attention": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
                 "bi_packed_weight_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
                 "bi_pack_weight": ([ptr, ctypes.c_void_p, ctypes.c_int64,
                                     ctypes.POINTER(BiPackedWeightDesc), ctypes.c_void_p], st),
@@ -281,6 +282,20 @@ def bi_mean_lastdim(x: torch.Tensor, out: torch.Tensor | None = None,
         out = torch.empty((x.shape[0],), dtype=out_dtype, device=x.device)
     dx, dy = _desc(x, "x"), _desc(out, "out")
     _check(lib, "bi_mean_lastdim", lib.bi_mean_lastdim(_ref(dx), _ref(dy), _stream(stream)))
+    return out
+
+
+def bi_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+                 out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                 stream=None) -> torch.Tensor:
+    """Fused attention softmax(scale * q k^T) v per head: q [L, Tq, 256], k / v
+    [L, Tk, 256] bf16; returns [L, Tq, 256] (fp32 unless out / out_dtype)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=out_dtype, device=q.device)
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out")
+    _check(lib, "bi_attention",
+           lib.bi_attention(_ref(dq), _ref(dk), _ref(dv), ctypes.c_float(scale), _ref(do), _stream(stream)))
     return out
 
 

@@ -784,6 +784,60 @@ extern "C" bi_status bi_mean_lastdim(const bi_tensor* x, const bi_tensor* y, bi_
   return run_rows(kRowMean, rp, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Fused attention
+// ---------------------------------------------------------------------------
+extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                                  const bi_tensor* o, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if ((st = check_tensor(q, "q", 3, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(k, "k", 3, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(v, "v", 3, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(o, "o", 3, &why)) != BI_OK) return finish(st, why);
+  const int64_t L = q->shape[0], Tq = q->shape[1], D = q->shape[2], Tk = k->shape[1];
+  if (k->shape[0] != L || k->shape[2] != D || v->shape[0] != L || v->shape[1] != Tk || v->shape[2] != D)
+    return finish(BI_ERR_SHAPE_MISMATCH, "k and v must be [L, Tk, D] with q's L and D");
+  if (o->shape[0] != L || o->shape[1] != Tq || o->shape[2] != D)
+    return finish(BI_ERR_SHAPE_MISMATCH, "o must be [L, Tq, D]");
+  if (q->dtype != BI_BF16 || k->dtype != BI_BF16 || v->dtype != BI_BF16)
+    return finish(BI_ERR_UNSUPPORTED_DTYPE, "q, k and v must be bf16");
+  if (o->dtype != BI_F32 && o->dtype != BI_BF16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "o must be fp32 or bf16");
+  if (D != 256) return finish(BI_ERR_INVALID_ARG, "head dimension must be 256");
+  if (!std::isfinite(scale)) return finish(BI_ERR_INVALID_ARG, "scale must be finite");
+  if (L == 0 || Tq == 0) return finish(BI_OK, why);
+  if (Tk == 0) return finish(BI_ERR_INVALID_ARG, "softmax over an empty key range is undefined");
+  const bi_tensor* ts[4] = {q, k, v, o};
+  for (int i = 0; i < 4; ++i) {
+    const bi_tensor* t = ts[i];
+    const int esz = elem_size(t->dtype);
+    if (t->stride[2] != 1) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "unit stride on the head dimension required");
+    if (!t->ptr) return finish(BI_ERR_INVALID_ARG, "null data pointer");
+    if (!aligned(t->ptr, 16)) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "base pointers must be 16-byte aligned");
+    if ((t->shape[1] > 1 && (t->stride[1] * esz) % 16 != 0) || (t->shape[0] > 1 && (t->stride[0] * esz) % 16 != 0))
+      return finish(BI_ERR_UNSUPPORTED_LAYOUT, "row and batch strides must be multiples of 16 bytes");
+  }
+  if ((L * ((Tq + 127) / 128)) > INT32_MAX) return finish(BI_ERR_INVALID_ARG, "too many query tiles");
+  // Strides of size-1 dimensions do not matter; give the tensor maps
+  // consistent ones.
+  auto st_t = [&](const bi_tensor* t) { return t->shape[1] > 1 ? t->stride[1] : D; };
+  auto st_l = [&](const bi_tensor* t) { return t->shape[0] > 1 ? t->stride[0] : t->shape[1] * st_t(t); };
+  AttnProblem ap;
+  ap.q = q->ptr;
+  ap.k = k->ptr;
+  ap.v = v->ptr;
+  ap.o = o->ptr;
+  ap.q_t = st_t(q), ap.q_l = st_l(q);
+  ap.k_t = st_t(k), ap.k_l = st_l(k);
+  ap.v_t = st_t(v), ap.v_l = st_l(v);
+  ap.o_t = st_t(o), ap.o_l = st_l(o);
+  ap.out_f32 = o->dtype == BI_F32;
+  ap.scale = scale;
+  ap.L = L, ap.Tq = Tq, ap.Tk = Tk, ap.D = D;
+  st = launch_attention(ap, (cudaStream_t)stream, &why);
+  return finish(st, why);
+}
+
 extern "C" bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
   std::string why;
   bi_status st;
@@ -829,7 +883,7 @@ extern "C" bi_status bi_device_status(bi_stream stream) {
   static const char* kSites[] = {"?", "producer waiting for a free stage", "MMA waiting for a full stage",
                                  "MMA waiting for a free accumulator", "epilogue waiting for an accumulator",
                                  "draining in-flight work", "debug wait", "conv producer waiting for a free stage",
-                                 "weight packer waiting for its tile"};
+                                 "weight packer waiting for its tile", "attention softmax waiting"};
   const unsigned site = (v >> 8) & 0xFF;
   why = std::string("device wait ran out: ") +
         (site < sizeof(kSites) / sizeof(kSites[0]) ? kSites[site] : "?");
@@ -860,4 +914,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 5; }
+extern "C" int32_t bi_abi_version(void) { return 6; }

@@ -1,0 +1,516 @@
+// bi_attn.cu -- fused attention o = softmax(scale * q k^T) v per head, in one
+// kernel, with a reduction order that no batch shape can change ("ai-infra
+// handbook: deterministic inference", section on fixed splitting, attention:
+// the key/value range is never split by load -- here it is not split at all,
+// one CTA walks every key of its query rows -- and a query row's result must
+// not depend on how the queries are chunked; "Batch-Invariant Kernel Design:
+// Conv2d and Attention BMM", section "Kernel 2: Attention BMM": every
+// flattened batch*head element is computed alone).
+//
+// Work unit: one head l and 128 consecutive query rows (a tile); a persistent
+// CTA takes tiles c, c + grid, ...  Per tile, for key blocks j = 0, 1, ... of
+// 128 keys in ascending order:
+//   S_j  = q k_j^T                    tcgen05.mma 128 x 128 x 16, 16 steps over D
+//                                      ascending, fp32 in TMEM (two S buffers)
+//   t    = RN(S_j * c),  c = RN(scale * log2 e);  keys >= Tk -> -inf
+//   m    = running row maximum of t, kept unless a block raises it by more
+//          than 8 (then O and the running sum are rescaled by 2^(m_old - m_new))
+//   p    = 2^(t - m) (SFU ex2),  l = RN(l * alpha) + sum p  (ascending keys)
+//   O   += bf16(p) v_j                tcgen05.mma 128 x 256 x 16, keys ascending,
+//                                      fp32 in TMEM
+// and finally o = RN(O * RN(1 / l)), rounded once to the output type.  Every
+// step is a function of the query row, the head's keys and values, Tk and
+// scale only: not of L, Tq, the tile a row falls in or the SM that runs it.
+//
+// Warps: 0 TMA producer (q tile once per tile, then K and V blocks through a
+// ring of four 32 KB stages), 1 MMA issuer (one thread), 2-5 softmax and
+// epilogue (one query row per thread; warp w reads TMEM lanes 32 (w % 4) ..).
+// Every wait is bounded; on expiry the kernel records the site, stops all
+// roles, drains what it issued and frees TMEM.
+#include <cuda_bf16.h>
+
+#include "bi_common.h"
+#include "bi_launch.h"
+#include "bi_roles.cuh"
+
+namespace bi {
+
+constexpr int kAttnBM = 128;  // query rows per tile
+constexpr int kAttnBN = 128;  // keys per block
+constexpr int kAttnD = 256;   // head dimension
+constexpr int kAttnStages = 4;
+constexpr int kAttnStageBytes = 32768;  // half a K block (128 keys x 128 D) or half a V block (64 keys x 256 D)
+constexpr int kAttnThreads = 192;
+constexpr uint32_t kAttnTmemCols = 512;  // S buffers at columns 0 and 128, O at 256
+constexpr uint32_t kAttnOCol = 256;
+constexpr float kAttnRescaleLog2 = 8.0f;  // keep a stale maximum while p <= 2^8
+
+struct AttnLayout {
+  static constexpr int Q = 0;                                       // 4 x [128 rows x 64 D]
+  static constexpr int P = Q + kAttnBM * kAttnD * 2;                // 2 x [128 rows x 64 keys]
+  static constexpr int STG = P + kAttnBM * kAttnBN * 2;             // stage ring
+  static constexpr int BARS = STG + kAttnStages * kAttnStageBytes;  // mbarriers
+  static constexpr int NBARS = 11 + 2 * kAttnStages;
+  static constexpr int SLOT = BARS + 8 * NBARS;  // TMEM address, abort flag
+  static constexpr int DYN = SLOT + 16 + 1024;   // + alignment slack
+};
+static_assert(AttnLayout::DYN <= 232448, "attention shared memory exceeds 227 KB");
+
+struct AttnBars {
+  uint32_t b;
+  __device__ __forceinline__ uint32_t q_full() const { return b; }
+  __device__ __forceinline__ uint32_t q_empty() const { return b + 8; }
+  __device__ __forceinline__ uint32_t full(uint32_t s) const { return b + 16 + 8 * s; }
+  __device__ __forceinline__ uint32_t empty(uint32_t s) const { return b + 16 + 8 * kAttnStages + 8 * s; }
+  __device__ __forceinline__ uint32_t s_full(uint32_t i) const { return b + 16 + 16 * kAttnStages + 8 * i; }
+  __device__ __forceinline__ uint32_t s_free(uint32_t i) const { return b + 32 + 16 * kAttnStages + 8 * i; }
+  __device__ __forceinline__ uint32_t p_full() const { return b + 48 + 16 * kAttnStages; }
+  __device__ __forceinline__ uint32_t pv_done() const { return b + 56 + 16 * kAttnStages; }
+  __device__ __forceinline__ uint32_t o_full() const { return b + 64 + 16 * kAttnStages; }
+  __device__ __forceinline__ uint32_t o_free() const { return b + 72 + 16 * kAttnStages; }
+  __device__ __forceinline__ uint32_t drain() const { return b + 80 + 16 * kAttnStages; }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// V halves (64 keys each) of key block j that hold at least one key < Tk;
+// a half wholly past Tk is neither loaded nor multiplied.
+__device__ __forceinline__ int attn_v_halves(int j, int Tk) {
+  return j * kAttnBN + kAttnBN / 2 < Tk ? 2 : 1;
+}
+
+// ---------------------------------------------------------------------------
+// Producer (one thread): per tile the q tile, then K_0, and for each block j
+// K_{j+1} (if any) followed by V_j -- the order the MMA issuer consumes them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBars& bars, uint32_t sQ,
+                                              uint32_t sS, const WaitCtl& wc) {
+  uint32_t it = 0;
+  int q_loads = 0;
+  bool ok = true;
+  auto next_stage = [&](uint32_t& dst, uint32_t& bar) -> bool {
+    const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+    if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word, wc.limit_ns,
+                                    status_code(6, kSiteProducerEmpty)))
+      return false;
+    dst = sS + s * kAttnStageBytes;
+    bar = bars.full(s);
+    mbar_arrive_expect_tx(bar, kAttnStageBytes);
+    ++it;
+    return true;
+  };
+  auto load_k = [&](int j, int l) -> bool {
+    for (int h = 0; h < 2; ++h) {
+      uint32_t dst, bar;
+      if (!next_stage(dst, bar)) return false;
+      for (int b = 0; b < 2; ++b) tma_load_3d(dst + b * 16384, &p.tma_k, bar, (2 * h + b) * 64, j * kAttnBN, l);
+    }
+    return true;
+  };
+  auto load_v = [&](int j, int l) -> bool {
+    const int halves = attn_v_halves(j, p.Tk);
+    for (int h = 0; h < halves; ++h) {
+      uint32_t dst, bar;
+      if (!next_stage(dst, bar)) return false;
+      for (int c = 0; c < 4; ++c)
+        tma_load_3d(dst + c * 8192, &p.tma_v, bar, c * 64, j * kAttnBN + h * (kAttnBN / 2), l);
+    }
+    return true;
+  };
+  for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+    const int l = tile / p.q_tiles;
+    const int q0 = (tile - l * p.q_tiles) * kAttnBM;
+    if (q_loads > 0 && !mbar_wait_bounded(bars.q_empty(), (q_loads - 1) & 1, wc.abort, wc.status_word,
+                                          wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
+      ok = false;
+      break;
+    }
+    mbar_arrive_expect_tx(bars.q_full(), kAttnBM * kAttnD * 2);
+    for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * 16384, &p.tma_q, bars.q_full(), c * 64, q0, l);
+    ++q_loads;
+    ok = load_k(0, l);
+    for (int j = 0; ok && j < p.kv_blocks; ++j) {
+      if (j + 1 < p.kv_blocks) ok = load_k(j + 1, l);
+      if (ok) ok = load_v(j, l);
+    }
+  }
+  // No copy may still be landing in shared memory when the CTA exits.
+  if (q_loads > 0)
+    mbar_wait_bounded(bars.q_full(), (q_loads - 1) & 1, nullptr, wc.status_word, wc.limit_ns,
+                      status_code(6, kSiteDrain));
+  const uint32_t first = it > (uint32_t)kAttnStages ? it - kAttnStages : 0u;
+  for (uint32_t j = first; j < it; ++j)
+    if (!mbar_wait_bounded(bars.full(j % kAttnStages), (j / kAttnStages) & 1, nullptr, wc.status_word,
+                           wc.limit_ns, status_code(6, kSiteDrain)))
+      break;
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread): S_0; then per block j: S_{j+1} (other S buffer),
+// PV_j once the softmax warps have written P_j.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& bars, uint32_t sQ, uint32_t sP,
+                                         uint32_t sS, uint32_t tmem, const WaitCtl& wc) {
+  const uint32_t kIdS = idesc_bf16_f32(kAttnBM, kAttnBN, false);
+  const uint32_t kIdO = idesc_bf16_f32(kAttnBM, kAttnD, true);
+  uint32_t it = 0, sc = 0, pc = 0;
+  int local = 0;
+  bool ok = true;
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return mbar_wait_bounded(bar, par, wc.abort, wc.status_word, wc.limit_ns, status_code(6, kSiteMmaFull));
+  };
+  auto issue_s = [&](int j) -> bool {
+    const uint32_t buf = sc & 1, use = sc >> 1;
+    if (use > 0 && !wait(bars.s_free(buf), (use - 1) & 1)) return false;
+    tc_fence_after_sync();
+    const uint32_t d = tmem + buf * kAttnBN;
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+      if (!wait(bars.full(s), r & 1)) return false;
+      tc_fence_after_sync();
+      const uint32_t kb = sS + s * kAttnStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int kq = 8 * h + kk;  // K = 16 step over D
+        const uint64_t ad = smem_desc_sw128(sQ + (kq >> 2) * 16384 + (kq & 3) * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        umma_bf16(d, ad, bd, kIdS, (h | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit(bars.empty(s));
+      ++it;
+    }
+    umma_commit(bars.s_full(buf));
+    ++sc;
+    if (j == p.kv_blocks - 1) umma_commit(bars.q_empty());  // the tile's last read of q
+    return true;
+  };
+  auto issue_pv = [&](int j) -> bool {
+    const int halves = attn_v_halves(j, p.Tk);
+    for (int h = 0; h < halves; ++h) {
+      const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+      if (!wait(bars.full(s), r & 1)) return false;
+      tc_fence_after_sync();
+      const uint32_t vb = sS + s * kAttnStageBytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // K = 16 step over keys
+        const uint64_t ad = smem_desc_sw128(sP + h * 16384 + k * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(vb + k * 2048, 64 * 128, 1024);
+        umma_bf16(tmem + kAttnOCol, ad, bd, kIdO, (j | h | k) != 0 ? 1u : 0u);
+      }
+      umma_commit(bars.empty(s));
+      ++it;
+    }
+    umma_commit(bars.pv_done());
+    ++pc;
+    return true;
+  };
+  for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+    if (!wait(bars.q_full(), local & 1)) break;
+    tc_fence_after_sync();
+    ok = issue_s(0);
+    for (int j = 0; ok && j < p.kv_blocks; ++j) {
+      if (j + 1 < p.kv_blocks) ok = issue_s(j + 1);
+      if (ok) ok = wait(bars.p_full(), pc & 1);
+      if (ok && j == 0 && local > 0) ok = wait(bars.o_free(), (local - 1) & 1);  // O is overwritten
+      if (ok) {
+        tc_fence_after_sync();
+        ok = issue_pv(j);
+      }
+    }
+    if (ok) umma_commit(bars.o_full());
+  }
+  // Every MMA issued above has finished before TMEM can be released.
+  umma_commit(bars.drain());
+  mbar_wait_bounded(bars.drain(), 0, nullptr, wc.status_word, wc.limit_ns, status_code(6, kSiteDrain));
+}
+
+// ---------------------------------------------------------------------------
+// Softmax and epilogue (warps 2-5): one query row per thread.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars& bars, uint32_t sP,
+                                             uint32_t tmem, int warp, int lane, const WaitCtl& wc) {
+  const int qd = warp & 3;  // TMEM lane quadrant this warp may access
+  const int row = qd * 32 + lane;
+  const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+  const float c2 = p.score_log2;
+  uint32_t sc = 0, pc = 0;
+  int local = 0;
+  auto wait_all = [&](uint32_t bar, uint32_t par) -> bool {
+    const bool got = mbar_wait_bounded(bar, par, wc.abort, wc.status_word, wc.limit_ns,
+                                       status_code(6, kSiteAttnSoftmax));
+    return __all_sync(0xffffffffu, got);
+  };
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+    const int l = tile / p.q_tiles;
+    const int q0 = (tile - l * p.q_tiles) * kAttnBM;
+    float m = -INFINITY, lsum = 0.0f;
+    for (int j = 0; j < p.kv_blocks; ++j) {
+      const uint32_t buf = sc & 1, use = sc >> 1;
+      if (!wait_all(bars.s_full(buf), use & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      float t[kAttnBN];
+#pragma unroll
+      for (int c = 0; c < kAttnBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32cols(trow + buf * kAttnBN + c * 32, r);
+        tmem_load_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[c * 32 + i] = __fmul_rn(__uint_as_float(r[i]), c2);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.s_free(buf));
+      ++sc;
+      const int kvalid = p.Tk - j * kAttnBN;  // keys of this block below Tk (>= 1)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kAttnBN; ++i) {
+        if (i >= kvalid) t[i] = -INFINITY;
+        mx = fmaxf(mx, t[i]);
+      }
+      const float m_new = fmaxf(m, mx);
+      float m_use = m, alpha = 1.0f;
+      bool resc = false;
+      if (j == 0) {
+        m_use = m_new;
+      } else if (m_new > __fadd_rn(m, kAttnRescaleLog2)) {
+        alpha = ex2_approx(__fsub_rn(m, m_new));
+        m_use = m_new;
+        resc = true;
+      }
+      uint32_t pk[kAttnBN / 2];
+      float ps = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kAttnBN; i += 2) {
+        const float p0 = ex2_approx(__fsub_rn(t[i], m_use));
+        const float p1 = ex2_approx(__fsub_rn(t[i + 1], m_use));
+        ps = __fadd_rn(ps, p0);
+        ps = __fadd_rn(ps, p1);
+        pk[i / 2] = pack_bf16x2(p0, p1);
+      }
+      lsum = __fadd_rn(resc ? __fmul_rn(lsum, alpha) : lsum, ps);
+      m = m_use;
+      // PV_{j-1} has finished: P may be overwritten and O is stable.
+      if (pc > 0 && !wait_all(bars.pv_done(), (pc - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (__any_sync(0xffffffffu, resc)) {
+        const float f = resc ? alpha : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < kAttnD / 32; ++c) {
+          uint32_t r[32];
+          tmem_load_32cols(trow + kAttnOCol + c * 32, r);
+          tmem_load_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), f));
+          tmem_store_32cols(trow + kAttnOCol + c * 32, r);
+        }
+        tmem_store_wait();
+      }
+      // P row into shared memory: K-major, 128-byte swizzle (16-byte unit u of
+      // row r stored at unit u ^ (r & 7)), keys 64h.. in half h.
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t addr = sP + h * 16384 + row * 128 + ((u ^ (row & 7)) << 4);
+          const int e = h * 32 + u * 4;
+          st_shared_v4(addr, pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
+        }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.p_full());
+      ++pc;
+    }
+    if (!ok) break;
+
+    // Epilogue: o = RN(O * RN(1 / l)), staged per warp in its own rows of the
+    // P buffer (free: every PV of the tile has completed) and stored by TMA.
+    if (!wait_all(bars.o_full(), local & 1)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    const float rinv = __frcp_rn(lsum);
+    const bool live = q0 + qd * 32 < p.Tq;  // warp-uniform: some of its rows are outputs
+    if (live) {
+      const int cols = p.out_f32 ? 32 : 64;  // columns per 128-byte staged row
+      for (int c = 0; c < kAttnD / cols; ++c) {
+        const uint32_t sbuf = sP + (c & 1) * 16384 + qd * 4096;
+        if (c >= 2) {
+          if (lane == 0) bulk_wait_read_1();
+          __syncwarp();
+        }
+        uint32_t w[32];
+        if (p.out_f32) {
+          uint32_t r[32];
+          tmem_load_32cols(trow + kAttnOCol + c * 32, r);
+          tmem_load_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), rinv));
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[32];
+            tmem_load_32cols(trow + kAttnOCol + c * 64 + hh * 32, r);
+            tmem_load_wait(r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[hh * 16 + i] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * i]), rinv),
+                                           __fmul_rn(__uint_as_float(r[2 * i + 1]), rinv));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(sbuf + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                       w[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tma_o, sbuf, c * cols, q0 + qd * 32, l);
+          bulk_commit();
+        }
+      }
+      if (lane == 0) bulk_wait_read_all();  // the rows may be P again in the next tile
+      __syncwarp();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.o_free());
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + AttnLayout::Q;
+  const uint32_t sP = base + AttnLayout::P;
+  const uint32_t sS = base + AttnLayout::STG;
+  const AttnBars bars{base + AttnLayout::BARS};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnLayout::SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full(), 1);
+    mbar_init(bars.q_empty(), 1);
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full(i), 1);
+      mbar_init(bars.s_free(i), 4);
+    }
+    mbar_init(bars.p_full(), 4);
+    mbar_init(bars.pv_done(), 1);
+    mbar_init(bars.o_full(), 1);
+    mbar_init(bars.o_free(), 4);
+    mbar_init(bars.drain(), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&p.tma_q);
+    tma_prefetch_desc(&p.tma_k);
+    tma_prefetch_desc(&p.tma_v);
+    tma_prefetch_desc(&p.tma_o);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kAttnTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.status_word, p.wait_limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) attn_producer(p, bars, sQ, sS, wc);
+  } else if (warp == 1) {
+    if (lane == 0) attn_mma(p, bars, sQ, sP, sS, tmem, wc);
+  } else {
+    attn_softmax(p, bars, sP, tmem, warp, lane, wc);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kAttnTmemCols);
+  }
+}
+
+bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why) {
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, why);
+  if (st != BI_OK) return st;
+  if (ap.D != kAttnD) {
+    *why = "head dimension must be 256";
+    return BI_ERR_INVALID_ARG;
+  }
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  auto map_in = [&](CUtensorMap* map, const void* ptr, int64_t T, int64_t st_t, int64_t st_l,
+                    uint32_t box_rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kAttnD, (cuuint64_t)T, (cuuint64_t)ap.L};
+    const cuuint64_t strides[2] = {(cuuint64_t)st_t * 2, (cuuint64_t)st_l * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    return encode_tiled_bf16(map, const_cast<void*>(ptr), 3, dims, strides, box, why);
+  };
+  if (!map_in(&p.tma_q, ap.q, ap.Tq, ap.q_t, ap.q_l, kAttnBM) ||
+      !map_in(&p.tma_k, ap.k, ap.Tk, ap.k_t, ap.k_l, kAttnBN) ||
+      !map_in(&p.tma_v, ap.v, ap.Tk, ap.v_t, ap.v_l, kAttnBN / 2))
+    return BI_ERR_CUDA;
+  {
+    const int esz = ap.out_f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)kAttnD, (cuuint64_t)ap.Tq, (cuuint64_t)ap.L};
+    const cuuint64_t strides[2] = {(cuuint64_t)(ap.o_t * esz), (cuuint64_t)(ap.o_l * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 32, 1};
+    if (!encode_tiled(&p.tma_o, ap.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B, ap.o, 3, dims, strides, box, why))
+      return BI_ERR_CUDA;
+  }
+  p.L = (int32_t)ap.L;
+  p.Tq = (int32_t)ap.Tq;
+  p.Tk = (int32_t)ap.Tk;
+  p.q_tiles = (int32_t)((ap.Tq + kAttnBM - 1) / kAttnBM);
+  p.kv_blocks = (int32_t)((ap.Tk + kAttnBN - 1) / kAttnBN);
+  const int64_t tiles = ap.L * (int64_t)p.q_tiles;
+  if (tiles > INT32_MAX) {
+    *why = "tile count exceeds 2^31";
+    return BI_ERR_INVALID_ARG;
+  }
+  p.num_tiles = (int32_t)tiles;
+  p.score_log2 = (float)((double)ap.scale * 1.4426950408889634);  // scale * log2(e)
+  p.out_f32 = ap.out_f32;
+  p.status_word = dev.status_word;
+  p.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attn_kernel), AttnLayout::DYN, 7);
+  if (e == cudaSuccess) {
+    const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
+    attn_kernel<<<grid, kAttnThreads, AttnLayout::DYN, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    *why = std::string("attention launch: ") + cudaGetErrorString(e);
+    return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
+}  // namespace bi

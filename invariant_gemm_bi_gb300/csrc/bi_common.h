@@ -38,6 +38,7 @@ enum : unsigned int {
   kSiteDebugWait = 6,
   kSiteConvProducer = 7,
   kSitePack = 8,
+  kSiteAttnSoftmax = 9,
 };
 __host__ __device__ constexpr unsigned int status_code(unsigned int bi_err, unsigned int site) {
   return bi_err | (site << 8);
@@ -103,6 +104,19 @@ struct PatchParams {
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;
   uint32_t stg_bytes;  // bytes of one staged K block of image rows (W * 4 * t_oh * 2)
   int32_t out_f32, bias_kind;
+  unsigned int* status_word;
+  uint64_t wait_limit_ns;
+};
+
+// Fused attention (bi_attn.cu): o[l] = softmax(scale * q[l] k[l]^T) v[l].
+struct AttnParams {
+  CUtensorMap tma_q;  // q as {D, Tq, L}, box {64, 128, 1}, 128B swizzle
+  CUtensorMap tma_k;  // k as {D, Tk, L}, box {64, 128, 1}
+  CUtensorMap tma_v;  // v as {D, Tk, L}, box {64, 64, 1}
+  CUtensorMap tma_o;  // o as {D, Tq, L}, box {128 bytes of D, 32, 1}
+  int32_t L, Tq, Tk, q_tiles, kv_blocks, num_tiles;
+  float score_log2;  // scale * log2(e), rounded once to fp32
+  int32_t out_f32;
   unsigned int* status_word;
   uint64_t wait_limit_ns;
 };

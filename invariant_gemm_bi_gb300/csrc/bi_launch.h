@@ -115,6 +115,19 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
 
 bi_status launch_softmax(const SoftmaxParams& sp, cudaStream_t stream, std::string* why);
 
+// Fused attention: q [L][Tq][256], k and v [L][Tk][256] bf16 (unit stride on
+// D, 16-byte row and batch strides), o [L][Tq][256] fp32 or bf16.
+struct AttnProblem {
+  const void *q, *k, *v;
+  int64_t q_t, q_l, k_t, k_l, v_t, v_l;  // element strides over T and L
+  void* o;
+  int64_t o_t, o_l;
+  int out_f32;
+  float scale;
+  int64_t L, Tq, Tk, D;
+};
+bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why);
+
 // op: kRowRmsNorm, kRowLogSoftmax or kRowMean.
 bi_status launch_row_reduction(int op, const RowParams& rp, cudaStream_t stream, std::string* why);
 

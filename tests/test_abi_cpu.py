@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 5
+    assert lib.bi_abi_version() == 6
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -266,3 +266,33 @@ def test_row_reduction_validation(lib):
                                                   None) == binding.BI_ERR_NO_DEVICE
                 assert lib.bi_mean_lastdim(_r(_t([4, 100], dtype=dx)), _r(_t([4], dtype=dy)),
                                            None) == binding.BI_ERR_NO_DEVICE
+
+
+def test_attention_validation(lib):
+    def call(q, k, v, o, scale=0.0625):
+        return lib.bi_attention(_r(q), _r(k), _r(v), ctypes.c_float(scale), _r(o), None)
+    q, k, v, o = _t([2, 100, 256]), _t([2, 90, 256]), _t([2, 90, 256]), _t([2, 100, 256], dtype=2)
+    # shapes
+    assert call(q, _t([2, 91, 256]), v, o) == binding.BI_ERR_SHAPE_MISMATCH
+    assert call(q, k, v, _t([2, 99, 256], dtype=2)) == binding.BI_ERR_SHAPE_MISMATCH
+    assert call(q, _t([3, 90, 256]), _t([3, 90, 256]), o) == binding.BI_ERR_SHAPE_MISMATCH
+    # head dimension 256 only; dtypes
+    assert call(_t([2, 100, 128]), _t([2, 90, 128]), _t([2, 90, 128]), _t([2, 100, 128], dtype=2)) == \
+        binding.BI_ERR_INVALID_ARG
+    assert call(_t([2, 100, 256], dtype=1), k, v, o) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    assert call(q, k, v, _t([2, 100, 256], dtype=1)) == binding.BI_ERR_UNSUPPORTED_DTYPE
+    # layouts: non-unit head stride, a row stride that is not 16 bytes, a misaligned base
+    assert call(_t([2, 100, 256], [256 * 100, 1, 100]), k, v, o) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert call(_t([2, 100, 256], [100 * 260, 260, 1]), k, v, o) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert call(q, _t([2, 90, 256], ptr=FAKE + 8), v, o) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    # scale must be finite; an empty key range has no softmax
+    assert call(q, k, v, o, float("inf")) == binding.BI_ERR_INVALID_ARG
+    assert call(q, _t([2, 0, 256]), _t([2, 0, 256]), o) == binding.BI_ERR_INVALID_ARG
+    # no query rows or no heads: nothing to do, before any CUDA call
+    assert call(_t([2, 0, 256]), k, v, _t([2, 0, 256], dtype=2)) == binding.BI_OK
+    assert call(_t([0, 100, 256]), _t([0, 90, 256]), _t([0, 90, 256]), _t([0, 100, 256], dtype=2)) == binding.BI_OK
+    # a valid call reaches the device check
+    import torch
+    if not torch.cuda.is_available():
+        assert call(q, k, v, o) == binding.BI_ERR_NO_DEVICE
+        assert call(q, k, v, _t([2, 100, 256], dtype=0)) == binding.BI_ERR_NO_DEVICE

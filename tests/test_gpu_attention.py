@@ -1,0 +1,152 @@
+"""GPU parity of the fused attention (bi_attention) against the fp64 oracle,
+and its invariances: a head computed alone or among any number of heads, and a
+query row computed among any other query rows, give the same bits ("ai-infra
+handbook: deterministic inference", section on fixed splitting: attention's
+key range is not split by load, and its result must not change with how
+queries are chunked; "Batch-Invariant Kernel Design: Conv2d and Attention
+BMM", section "Kernel 2: Attention BMM").
+
+Tolerance per output element, from the oracle's o = ref, absum = sum_j p_j |v_jd|
+and smax = |scale| max_j sum_d |q_d k_jd| of its row:
+    |o - ref| <= (2^-8 + 2.2e-4 smax + 2^-20 smax + 1e-4 + Tk 2^-23) absum + u_out |ref|
+2^-8: p is rounded to bf16 before it multiplies v (relative 2^-9, doubled for
+the normalisation it does not share); 1e-4 smax bounds the fp32 tensor-core
+error of a score (as the GEMM tests' 1e-4 sum |ab|), which moves a weight by
+that much relative, twice over (numerator and denominator); 2^-20 smax covers
+rounding the scaled score and the SFU's 2^x; 1e-4 the fp32 accumulation of
+P V; Tk 2^-23 the running sum of weights; u_out (2^-8 bf16, 2^-24 fp32) the
+final rounding.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_gemm_bi_gb300 import binding
+from invariant_gemm_bi_gb300 import inputs
+from tests.gpu_helpers import bits_equal
+
+pytestmark = pytest.mark.gpu
+
+U_OUT = {torch.bfloat16: 2.0 ** -8, torch.float32: 2.0 ** -24}
+D = 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    binding.load()
+    yield
+    assert binding.bi_device_status() == binding.BI_OK
+
+
+def _qkv(L, Tq, Tk, seed):
+    q = inputs.normal_bf16((L, Tq, D), 1.0, seed)
+    k = inputs.normal_bf16((L, Tk, D), 1.0, seed + 1)
+    v = inputs.normal_bf16((L, Tk, D), 1.0, seed + 2)
+    return q, k, v
+
+
+def check_attention(o: torch.Tensor, ref, absum, smax, Tk: int, what: str = ""):
+    g = o.detach().to("cpu", torch.float64).numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    sm = smax[..., None]
+    bound = (2.0 ** -8 + 2.2e-4 * sm + 2.0 ** -20 * sm + 1e-4 + Tk * 2.0 ** -23) * absum + \
+        U_OUT[o.dtype] * np.abs(ref)
+    err = np.abs(g - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        det = [(tuple(i), g[tuple(i)], ref[tuple(i)], bound[tuple(i)]) for i in idx]
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance, e.g. {det}")
+
+
+# (L, Tq, Tk): one query and one key; exactly one tile and one key block;
+# ragged tails in both; more keys than queries and the reverse; the
+# attention workload's sequence length (816 = 6 x 128 + 48)
+SHAPES = [(1, 1, 1), (1, 128, 128), (2, 129, 64), (3, 200, 333), (1, 50, 1000), (2, 816, 816)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_attention_matches_oracle(shape, out_dtype):
+    L, Tq, Tk = shape
+    q, k, v = _qkv(L, Tq, Tk, 10)
+    ref, absum, smax = oracle.attention(q, k, v, 1.0 / 16)
+    o = binding.bi_attention(q.cuda(), k.cuda(), v.cuda(), 1.0 / 16, out_dtype=out_dtype)
+    check_attention(o, ref, absum, smax, Tk, f"attention {shape} -> {out_dtype}")
+
+
+@pytest.mark.parametrize("rising", [True, False])
+def test_attention_running_maximum_rescales(rising):
+    # scores that climb by ~20 per block (~30 in log2 units) force the running maximum to move
+    # (and O and the running sum to be rescaled) at every block; falling
+    # scores never move it after the first block
+    L, Tq, Tk = 2, 130, 700
+    q = (torch.ones(L, Tq, D) * 0.25).to(torch.bfloat16)
+    ramp = torch.arange(Tk, dtype=torch.float32) / 10.0
+    if not rising:
+        ramp = ramp.flip(0)
+    k = (ramp[None, :, None] * torch.ones(L, Tk, D)).to(torch.bfloat16)
+    k[:, :, 1::2] *= -0.5                                   # vary the scores' mix of signs
+    v = inputs.normal_bf16((L, Tk, D), 1.0, 20)
+    ref, absum, smax = oracle.attention(q, k, v, 0.1)
+    o = binding.bi_attention(q.cuda(), k.cuda(), v.cuda(), 0.1)
+    check_attention(o, ref, absum, smax, Tk, f"rescale rising={rising}")
+
+
+def test_attention_head_alone_equals_head_in_batch():
+    # head 0 of sample 0 alone vs among 16 heads, with distractor heads full
+    # of huge, infinite and NaN values
+    q, k, v = _qkv(16, 300, 300, 30)
+    q[5], k[6], v[7] = 2.0 ** 100, float("inf"), float("nan")
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    full = binding.bi_attention(qg, kg, vg, 1.0 / 16)
+    for L in (1, 2, 8):
+        assert bits_equal(binding.bi_attention(qg[:L], kg[:L], vg[:L], 1.0 / 16), full[:L]), L
+    assert bits_equal(binding.bi_attention(qg[3:4], kg[3:4], vg[3:4], 1.0 / 16), full[3:4])
+    ref, absum, smax = oracle.attention(q[:2], k[:2], v[:2], 1.0 / 16)
+    check_attention(full[:2], ref, absum, smax, 300, "head 0/1 among distractors")
+    # and run to run
+    assert bits_equal(binding.bi_attention(qg, kg, vg, 1.0 / 16), full)
+
+
+def test_attention_query_chunking_invariance():
+    # a query row gives the same bits whatever other query rows come with it
+    # and wherever it falls in a 128-row tile (chunked prefill)
+    q, k, v = _qkv(2, 400, 500, 40)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    full = binding.bi_attention(qg, kg, vg, 1.0 / 16)
+    for a, b in ((0, 1), (0, 300), (50, 400), (127, 129), (399, 400), (200, 333)):
+        part = binding.bi_attention(qg[:, a:b].contiguous(), kg, vg, 1.0 / 16)
+        assert bits_equal(part, full[:, a:b]), (a, b)
+
+
+def test_attention_strided_inputs_and_output():
+    # q, k, v as views of one packed [L, T, 3, 256] tensor (row stride 768),
+    # output into a padded buffer: the same bits as contiguous operands
+    L, T = 3, 250
+    qkv = inputs.normal_bf16((L, T, 3, D), 1.0, 50)
+    g = qkv.cuda()
+    q, k, v = g[:, :, 0], g[:, :, 1], g[:, :, 2]
+    ref_o = binding.bi_attention(q.contiguous(), k.contiguous(), v.contiguous(), 0.0625)
+    big = torch.full((L, T + 3, D + 64), 7.0, device="cuda")
+    out = big[:, 1:T + 1, 32:32 + D]
+    binding.bi_attention(q, k, v, 0.0625, out=out)
+    assert bits_equal(out.contiguous(), ref_o)
+    assert bool((big[:, 0] == 7.0).all()) and bool((big[:, T + 1:] == 7.0).all())
+    assert bool((big[:, :, :32] == 7.0).all()) and bool((big[:, :, 32 + D:] == 7.0).all())
+
+
+def test_attention_workload_sampled_heads():
+    # the timed shape at B = 32: Q, K, V [256, 816, 256]; heads 0, 100 and 255
+    # against the oracle, head 0 bit-equal to the B = 1 run
+    q, k, v = inputs.attention(32)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    o = binding.bi_attention(qg, kg, vg, 1.0 / 16)
+    for h in (0, 100, 255):
+        ref, absum, smax = oracle.attention(q[h:h + 1], k[h:h + 1], v[h:h + 1], 1.0 / 16)
+        check_attention(o[h:h + 1], ref, absum, smax, 816, f"B=32 head {h}")
+    o1 = binding.bi_attention(qg[:8], kg[:8], vg[:8], 1.0 / 16)
+    assert bits_equal(o1, o[:8])
