@@ -406,7 +406,7 @@ def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
 def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
     # S = QK^T/16 (fp32), P = softmax(S) (bf16), O = PV (fp32)
     q, k, v = inputs.attention(max(inputs.ATTENTION_B), device="cuda")
-    res, o0 = [], {}
+    res, o0, of0, sd0 = [], {}, {}, {}
     for B in inputs.ATTENTION_B:
         L = 8 * B
         qb, kb, vb = q[:L], k[:L].transpose(1, 2), v[:L]
@@ -423,12 +423,25 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         b2 = L * 816 * 816 * 6.0
         b3 = L * (2.0 * 816 * 816 + 2.0 * 816 * 256 + 4.0 * 816 * 256)
         tcb = measure(lambda: torch.bmm(qb, kb), flush_buf, stream, reps)
-        res.append({"B": B, "qk": point(f1, b1, t1),
+        # the same attention fused in one kernel (fp32 out), and PyTorch's SDPA
+        of = torch.empty(L, 816, 256, dtype=torch.float32, device="cuda")
+        tf = measure(lambda: binding.bi_attention(qb, k[:L], vb, 1.0 / 16, out=of), flush_buf, stream, reps)
+        of0[B] = of[:1].clone()
+        ff = 2 * f1
+        bf = L * (3 * 2.0 * 816 * 256 + 4.0 * 816 * 256)
+        tsd = measure(lambda: torch.nn.functional.scaled_dot_product_attention(qb, k[:L], vb, scale=1.0 / 16),
+                      flush_buf, stream, reps)
+        sd0[B] = torch.nn.functional.scaled_dot_product_attention(qb, k[:L], vb, scale=1.0 / 16)[:1].clone()
+        fused = {**point(ff, bf, tf), "sdpa_us_bf16_out": round(tsd * 1e6, 2)}
+        del of
+        res.append({"B": B, "fused": fused, "qk": point(f1, b1, t1),
                     "softmax": {"us": round(t2 * 1e6, 2), "gbs": round(b2 / t2 / 1e9, 1),
                                 "roofline_frac": round(b2 / (peaks["hbm_gbs"] * 1e9) / t2, 3), "bound": "hbm"},
                     "pv": point(f1, b3, t3), "cublas_qk_us": round(tcb * 1e6, 2)})
         del s, p, o
-    out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0)}
+    out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0),
+                        "fused_head0_bit_equal_all_B": all(bits_equal(of0[B], of0[1]) for B in of0),
+                        "sdpa_head0_bit_equal_all_B": all(bits_equal(sd0[B], sd0[1]) for B in sd0)}
     del q, k, v
 
 

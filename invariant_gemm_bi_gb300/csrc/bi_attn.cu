@@ -15,7 +15,10 @@
 //   t    = RN(S_j * c),  c = RN(scale * log2 e);  keys >= Tk -> -inf
 //   m    = running row maximum of t, kept unless a block raises it by more
 //          than 8 (then O and the running sum are rescaled by 2^(m_old - m_new))
-//   p    = 2^(t - m) (SFU ex2),  l = RN(l * alpha) + sum p  (ascending keys)
+//   p    = 2^(t - m) (SFU ex2)
+//   l_h  = RN(l_h * alpha) + ((a0 + a1) + (a2 + a3)) for each half h of the
+//          block (keys 0-63, 64-127), a_r the sum of the half's p with key
+//          index = r mod 4, ascending;  l = l_0 + l_1 at the end
 //   O   += bf16(p) v_j                tcgen05.mma 128 x 256 x 16, keys ascending,
 //                                      fp32 in TMEM
 // and finally o = RN(O * RN(1 / l)), rounded once to the output type.  Every
@@ -23,8 +26,13 @@
 // scale only: not of L, Tq, the tile a row falls in or the SM that runs it.
 //
 // Warps: 0 TMA producer (q tile once per tile, then K and V blocks through a
-// ring of four 32 KB stages), 1 MMA issuer (one thread), 2-5 softmax and
-// epilogue (one query row per thread; warp w reads TMEM lanes 32 (w % 4) ..).
+// ring of 128 KB of stages), 1 MMA issuer (one thread), 2-9 softmax and
+// epilogue: warps w and w + 4 share the 32 query rows of TMEM lane quadrant
+// w % 4, one row per thread; warps 2-5 take keys 0-63 of each block and O
+// columns 0-127, warps 6-9 keys 64-127 and O columns 128-255.  The two warps
+// of a quadrant exchange their block maxima through a TMEM column of the S
+// buffer they have consumed, and decide every wait together (a barrier that
+// ANDs their outcomes), so they always take the same path.
 // Every wait is bounded; on expiry the kernel records the site, stops all
 // roles, drains what it issued and frees TMEM.
 #include <cuda_bf16.h>
@@ -38,9 +46,17 @@ namespace bi {
 constexpr int kAttnBM = 128;  // query rows per tile
 constexpr int kAttnBN = 128;  // keys per block
 constexpr int kAttnD = 256;   // head dimension
-constexpr int kAttnStages = 4;
-constexpr int kAttnStageBytes = 32768;  // half a K block (128 keys x 128 D) or half a V block (64 keys x 256 D)
-constexpr int kAttnThreads = 192;
+#ifndef BI_ATTN_STAGE_KB
+#define BI_ATTN_STAGE_KB 32
+#endif
+// A stage holds kAttnKC 16 KB pieces: of a K block, D columns of 64 for all
+// 128 keys; of a V block, 32 keys with all 256 D columns.
+constexpr int kAttnKC = BI_ATTN_STAGE_KB / 16;
+constexpr int kAttnStageBytes = kAttnKC * 16384;
+constexpr int kAttnStages = 131072 / kAttnStageBytes;
+constexpr int kAttnVKeys = 32 * kAttnKC;  // keys of V per stage
+constexpr int kAttnThreads = 320;
+constexpr int kAttnSoftmaxWarps = 8;
 constexpr uint32_t kAttnTmemCols = 512;  // S buffers at columns 0 and 128, O at 256
 constexpr uint32_t kAttnOCol = 256;
 constexpr float kAttnRescaleLog2 = 8.0f;  // keep a stale maximum while p <= 2^8
@@ -51,7 +67,8 @@ struct AttnLayout {
   static constexpr int STG = P + kAttnBM * kAttnBN * 2;             // stage ring
   static constexpr int BARS = STG + kAttnStages * kAttnStageBytes;  // mbarriers
   static constexpr int NBARS = 11 + 2 * kAttnStages;
-  static constexpr int SLOT = BARS + 8 * NBARS;  // TMEM address, abort flag
+  static constexpr int XCH = BARS + 8 * NBARS;    // running-sum exchange, 2 x 128 floats
+  static constexpr int SLOT = XCH + 2 * kAttnBM * 4;  // TMEM address, abort flag
   static constexpr int DYN = SLOT + 16 + 1024;   // + alignment slack
 };
 static_assert(AttnLayout::DYN <= 232448, "attention shared memory exceeds 227 KB");
@@ -72,14 +89,16 @@ struct AttnBars {
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// V halves (64 keys each) of key block j that hold at least one key < Tk;
-// a half wholly past Tk is neither loaded nor multiplied.
-__device__ __forceinline__ int attn_v_halves(int j, int Tk) {
-  return j * kAttnBN + kAttnBN / 2 < Tk ? 2 : 1;
+// V stages (kAttnVKeys keys each) of key block j that hold at least one key
+// < Tk; a stage's worth of keys wholly past Tk is neither loaded nor
+// multiplied.
+__device__ __forceinline__ int attn_v_stages(int j, int Tk) {
+  const int left = Tk - j * kAttnBN;
+  return left >= kAttnBN ? kAttnBN / kAttnVKeys : (left + kAttnVKeys - 1) / kAttnVKeys;
 }
 
 // ---------------------------------------------------------------------------
@@ -102,21 +121,22 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
     ++it;
     return true;
   };
-  auto load_k = [&](int j, int l) -> bool {
-    for (int h = 0; h < 2; ++h) {
+  auto load_k = [&](int j, int l) -> bool {  // all keys of block j, D columns 64c.. per piece
+    for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
-      for (int b = 0; b < 2; ++b) tma_load_3d(dst + b * 16384, &p.tma_k, bar, (2 * h + b) * 64, j * kAttnBN, l);
+      for (int b = 0; b < kAttnKC; ++b)
+        tma_load_3d(dst + b * 16384, &p.tma_k, bar, (cs * kAttnKC + b) * 64, j * kAttnBN, l);
     }
     return true;
   };
-  auto load_v = [&](int j, int l) -> bool {
-    const int halves = attn_v_halves(j, p.Tk);
-    for (int h = 0; h < halves; ++h) {
+  auto load_v = [&](int j, int l) -> bool {  // kAttnVKeys keys of block j per stage, all D
+    const int nst = attn_v_stages(j, p.Tk);
+    for (int vs = 0; vs < nst; ++vs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
       for (int c = 0; c < 4; ++c)
-        tma_load_3d(dst + c * 8192, &p.tma_v, bar, c * 64, j * kAttnBN + h * (kAttnBN / 2), l);
+        tma_load_3d(dst + c * (kAttnVKeys * 128), &p.tma_v, bar, c * 64, j * kAttnBN + vs * kAttnVKeys, l);
     }
     return true;
   };
@@ -167,17 +187,20 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
     if (use > 0 && !wait(bars.s_free(buf), (use - 1) & 1)) return false;
     tc_fence_after_sync();
     const uint32_t d = tmem + buf * kAttnBN;
-    for (int h = 0; h < 2; ++h) {
+    for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
       const uint32_t s = it % kAttnStages, r = it / kAttnStages;
       if (!wait(bars.full(s), r & 1)) return false;
       tc_fence_after_sync();
       const uint32_t kb = sS + s * kAttnStageBytes;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int kq = 8 * h + kk;  // K = 16 step over D
-        const uint64_t ad = smem_desc_sw128(sQ + (kq >> 2) * 16384 + (kq & 3) * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        umma_bf16(d, ad, bd, kIdS, (h | kk) != 0 ? 1u : 0u);
+      for (int b = 0; b < kAttnKC; ++b) {
+        const int c = cs * kAttnKC + b;  // D columns 64c..
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // K = 16 steps over D, ascending
+          const uint64_t ad = smem_desc_sw128(sQ + c * 16384 + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + b * 16384 + kk * 32, 16, 1024);
+          umma_bf16(d, ad, bd, kIdS, (c | kk) != 0 ? 1u : 0u);
+        }
       }
       umma_commit(bars.empty(s));
       ++it;
@@ -188,17 +211,18 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
     return true;
   };
   auto issue_pv = [&](int j) -> bool {
-    const int halves = attn_v_halves(j, p.Tk);
-    for (int h = 0; h < halves; ++h) {
+    const int nst = attn_v_stages(j, p.Tk);
+    for (int vs = 0; vs < nst; ++vs) {  // keys vs * kAttnVKeys.. of the block
       const uint32_t s = it % kAttnStages, r = it / kAttnStages;
       if (!wait(bars.full(s), r & 1)) return false;
       tc_fence_after_sync();
       const uint32_t vb = sS + s * kAttnStageBytes;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // K = 16 step over keys
-        const uint64_t ad = smem_desc_sw128(sP + h * 16384 + k * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(vb + k * 2048, 64 * 128, 1024);
-        umma_bf16(tmem + kAttnOCol, ad, bd, kIdO, (j | h | k) != 0 ? 1u : 0u);
+      for (int k = 0; k < kAttnVKeys / 16; ++k) {  // K = 16 steps over keys, ascending
+        const int key = vs * kAttnVKeys + 16 * k;  // first key of the step within the block
+        const uint64_t ad = smem_desc_sw128(sP + (key >> 6) * 16384 + ((key & 63) >> 4) * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(vb + k * 2048, kAttnVKeys * 128, 1024);
+        umma_bf16(tmem + kAttnOCol, ad, bd, kIdO, (j | vs | k) != 0 ? 1u : 0u);
       }
       umma_commit(bars.empty(s));
       ++it;
@@ -228,20 +252,24 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
 }
 
 // ---------------------------------------------------------------------------
-// Softmax and epilogue (warps 2-5): one query row per thread.
+// Softmax and epilogue (warps 2-9): one query row and one half of the keys /
+// of O's columns per thread.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars& bars, uint32_t sP,
-                                             uint32_t tmem, int warp, int lane, const WaitCtl& wc) {
-  const int qd = warp & 3;  // TMEM lane quadrant this warp may access
+                                             float* xch, uint32_t tmem, int warp, int lane, const WaitCtl& wc) {
+  const int qd = warp & 3;         // TMEM lane quadrant this warp may access
+  const int hc = (warp - 2) >> 2;  // half: keys 64hc.. of a block, O columns 128hc..
   const int row = qd * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+  const uint32_t pair_bar = 1 + qd;  // named barrier of the quadrant's two warps
   const float c2 = p.score_log2;
   uint32_t sc = 0, pc = 0;
   int local = 0;
-  auto wait_all = [&](uint32_t bar, uint32_t par) -> bool {
+  // Both warps of the quadrant wait, then agree: true only if both got it.
+  auto wait_pair = [&](uint32_t bar, uint32_t par) -> bool {
     const bool got = mbar_wait_bounded(bar, par, wc.abort, wc.status_word, wc.limit_ns,
                                        status_code(6, kSiteAttnSoftmax));
-    return __all_sync(0xffffffffu, got);
+    return named_barrier_and(pair_bar, 64, got);
   };
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
@@ -250,32 +278,54 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     float m = -INFINITY, lsum = 0.0f;
     for (int j = 0; j < p.kv_blocks; ++j) {
       const uint32_t buf = sc & 1, use = sc >> 1;
-      if (!wait_all(bars.s_full(buf), use & 1)) {
+      if (!wait_pair(bars.s_full(buf), use & 1)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      float t[kAttnBN];
+      const uint32_t scol = trow + buf * kAttnBN + hc * 64;
+      float t[64];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_load_32cols(scol, r0);
+        tmem_load_32cols(scol + 32, r1);
+        tmem_load_wait(r0);
+        tmem_load_wait(r1);
 #pragma unroll
-      for (int c = 0; c < kAttnBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_load_32cols(trow + buf * kAttnBN + c * 32, r);
-        tmem_load_wait(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) t[c * 32 + i] = __fmul_rn(__uint_as_float(r[i]), c2);
+        for (int i = 0; i < 32; ++i) {
+          t[i] = __fmul_rn(__uint_as_float(r0[i]), c2);
+          t[32 + i] = __fmul_rn(__uint_as_float(r1[i]), c2);
+        }
       }
+      const int kvalid = p.Tk - j * kAttnBN - hc * 64;  // keys of this half below Tk
+      if (kvalid < 64) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i >= kvalid) t[i] = -INFINITY;
+      }
+      float mx;
+      {
+        float mp[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) mp[r] = t[r];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], t[i]);
+        mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      }
+      // Exchange the halves' maxima through the first column of each half of
+      // the consumed S buffer, then release the buffer.
+      tmem_store_1col(scol, __float_as_uint(mx));
+      tmem_store_wait();
+      tc_fence_before_sync();
+      named_barrier(pair_bar, 64);
+      tc_fence_after_sync();
+      const float mo = __uint_as_float(tmem_load_1col(trow + buf * kAttnBN + (1 - hc) * 64));
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.s_free(buf));
       ++sc;
-      const int kvalid = p.Tk - j * kAttnBN;  // keys of this block below Tk (>= 1)
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kAttnBN; ++i) {
-        if (i >= kvalid) t[i] = -INFINITY;
-        mx = fmaxf(mx, t[i]);
-      }
-      const float m_new = fmaxf(m, mx);
+      const float m_blk = hc == 0 ? fmaxf(mx, mo) : fmaxf(mo, mx);  // the same operands in both warps
+      const float m_new = fmaxf(m, m_blk);
       float m_use = m, alpha = 1.0f;
       bool resc = false;
       if (j == 0) {
@@ -285,20 +335,21 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         m_use = m_new;
         resc = true;
       }
-      uint32_t pk[kAttnBN / 2];
-      float ps = 0.0f;
+      uint32_t pk[32];
+      float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int i = 0; i < kAttnBN; i += 2) {
+      for (int i = 0; i < 64; i += 2) {
         const float p0 = ex2_approx(__fsub_rn(t[i], m_use));
         const float p1 = ex2_approx(__fsub_rn(t[i + 1], m_use));
-        ps = __fadd_rn(ps, p0);
-        ps = __fadd_rn(ps, p1);
+        a4[i & 3] = __fadd_rn(a4[i & 3], p0);
+        a4[(i + 1) & 3] = __fadd_rn(a4[(i + 1) & 3], p1);
         pk[i / 2] = pack_bf16x2(p0, p1);
       }
+      const float ps = __fadd_rn(__fadd_rn(a4[0], a4[1]), __fadd_rn(a4[2], a4[3]));
       lsum = __fadd_rn(resc ? __fmul_rn(lsum, alpha) : lsum, ps);
       m = m_use;
       // PV_{j-1} has finished: P may be overwritten and O is stable.
-      if (pc > 0 && !wait_all(bars.pv_done(), (pc - 1) & 1)) {
+      if (pc > 0 && !wait_pair(bars.pv_done(), (pc - 1) & 1)) {
         ok = false;
         break;
       }
@@ -306,26 +357,23 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
       if (__any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < kAttnD / 32; ++c) {
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t oc = trow + kAttnOCol + hc * 128 + c * 32;
           uint32_t r[32];
-          tmem_load_32cols(trow + kAttnOCol + c * 32, r);
+          tmem_load_32cols(oc, r);
           tmem_load_wait(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), f));
-          tmem_store_32cols(trow + kAttnOCol + c * 32, r);
+          tmem_store_32cols(oc, r);
         }
         tmem_store_wait();
       }
-      // P row into shared memory: K-major, 128-byte swizzle (16-byte unit u of
-      // row r stored at unit u ^ (r & 7)), keys 64h.. in half h.
+      // This half's P row into shared memory: K-major, 128-byte swizzle
+      // (16-byte unit u of row r stored at unit u ^ (r & 7)).
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t addr = sP + h * 16384 + row * 128 + ((u ^ (row & 7)) << 4);
-          const int e = h * 32 + u * 4;
-          st_shared_v4(addr, pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
-        }
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(sP + hc * 16384 + row * 128 + ((u ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                     pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
@@ -334,27 +382,30 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     }
     if (!ok) break;
 
-    // Epilogue: o = RN(O * RN(1 / l)), staged per warp in its own rows of the
-    // P buffer (free: every PV of the tile has completed) and stored by TMA.
-    if (!wait_all(bars.o_full(), local & 1)) {
+    // Epilogue: o = RN(O * RN(1 / (l_0 + l_1))).  Each warp turns its 32 rows
+    // x 128 columns around through its own 4 KB of the P buffer (every PV of
+    // the tile has completed), 128 bytes of each row at a time, so that each
+    // global store instruction writes four whole 128-byte row segments.
+    if (!wait_pair(bars.o_full(), local & 1)) {
       ok = false;
       break;
     }
     tc_fence_after_sync();
-    const float rinv = __frcp_rn(lsum);
-    const bool live = q0 + qd * 32 < p.Tq;  // warp-uniform: some of its rows are outputs
-    if (live) {
-      const int cols = p.out_f32 ? 32 : 64;  // columns per 128-byte staged row
-      for (int c = 0; c < kAttnD / cols; ++c) {
-        const uint32_t sbuf = sP + (c & 1) * 16384 + qd * 4096;
-        if (c >= 2) {
-          if (lane == 0) bulk_wait_read_1();
-          __syncwarp();
-        }
+    xch[hc * kAttnBM + row] = lsum;
+    named_barrier(pair_bar, 64);
+    const float lo = xch[(1 - hc) * kAttnBM + row];
+    named_barrier(pair_bar, 64);  // both read before the next tile writes again
+    const float rinv = __frcp_rn(hc == 0 ? __fadd_rn(lsum, lo) : __fadd_rn(lo, lsum));
+    if (q0 + qd * 32 < p.Tq) {  // warp-uniform: some of its rows are outputs
+      const uint32_t region = sP + hc * 16384 + qd * 4096;
+      const int esz = p.out_f32 ? 4 : 2;
+      const int cols = 128 / esz;  // columns per 128-byte piece of a row
+      char* obase = static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)(q0 + qd * 32) * p.o_t) * esz;
+      for (int c = 0; c < 128 / cols; ++c) {
         uint32_t w[32];
         if (p.out_f32) {
           uint32_t r[32];
-          tmem_load_32cols(trow + kAttnOCol + c * 32, r);
+          tmem_load_32cols(trow + kAttnOCol + hc * 128 + c * 32, r);
           tmem_load_wait(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), rinv));
@@ -362,7 +413,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t r[32];
-            tmem_load_32cols(trow + kAttnOCol + c * 64 + hh * 32, r);
+            tmem_load_32cols(trow + kAttnOCol + hc * 128 + c * 64 + hh * 32, r);
             tmem_load_wait(r);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -370,25 +421,29 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
                                            __fmul_rn(__uint_as_float(r[2 * i + 1]), rinv));
           }
         }
+        __syncwarp();  // the previous piece has been read back
+        // row `lane`, 16-byte unit u at unit u ^ (lane & 7): conflict-free both ways
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          st_shared_v4(sbuf + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+          st_shared_v4(region + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
                        w[4 * u + 3]);
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&p.tma_o, sbuf, c * cols, q0 + qd * 32, l);
-          bulk_commit();
+        // read back: lane L takes unit L % 8 of rows 4i + L / 8
+        const int u = lane & 7;
+        const int col = hc * 128 + c * cols + u * (16 / esz);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const uint4 v = ld_shared_v4(region + rr * 128 + ((u ^ (rr & 7)) << 4));
+          if (q0 + qd * 32 + rr < p.Tq)
+            *reinterpret_cast<uint4*>(obase + ((int64_t)rr * p.o_t + col) * esz) = v;
         }
       }
-      if (lane == 0) bulk_wait_read_all();  // the rows may be P again in the next tile
-      __syncwarp();
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.o_free());
   }
-  if (lane == 0) bulk_wait_all();
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
@@ -414,19 +469,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full(i), 1);
-      mbar_init(bars.s_free(i), 4);
+      mbar_init(bars.s_free(i), kAttnSoftmaxWarps);
     }
-    mbar_init(bars.p_full(), 4);
+    mbar_init(bars.p_full(), kAttnSoftmaxWarps);
     mbar_init(bars.pv_done(), 1);
     mbar_init(bars.o_full(), 1);
-    mbar_init(bars.o_free(), 4);
+    mbar_init(bars.o_free(), kAttnSoftmaxWarps);
     mbar_init(bars.drain(), 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&p.tma_q);
     tma_prefetch_desc(&p.tma_k);
     tma_prefetch_desc(&p.tma_v);
-    tma_prefetch_desc(&p.tma_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kAttnTmemCols);
@@ -443,7 +497,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   } else if (warp == 1) {
     if (lane == 0) attn_mma(p, bars, sQ, sP, sS, tmem, wc);
   } else {
-    attn_softmax(p, bars, sP, tmem, warp, lane, wc);
+    attn_softmax(p, bars, sP, reinterpret_cast<float*>(smem + AttnLayout::XCH), tmem, warp, lane, wc);
   }
 
   tc_fence_before_sync();
@@ -474,17 +528,11 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   };
   if (!map_in(&p.tma_q, ap.q, ap.Tq, ap.q_t, ap.q_l, kAttnBM) ||
       !map_in(&p.tma_k, ap.k, ap.Tk, ap.k_t, ap.k_l, kAttnBN) ||
-      !map_in(&p.tma_v, ap.v, ap.Tk, ap.v_t, ap.v_l, kAttnBN / 2))
+      !map_in(&p.tma_v, ap.v, ap.Tk, ap.v_t, ap.v_l, kAttnVKeys))
     return BI_ERR_CUDA;
-  {
-    const int esz = ap.out_f32 ? 4 : 2;
-    const cuuint64_t dims[3] = {(cuuint64_t)kAttnD, (cuuint64_t)ap.Tq, (cuuint64_t)ap.L};
-    const cuuint64_t strides[2] = {(cuuint64_t)(ap.o_t * esz), (cuuint64_t)(ap.o_l * esz)};
-    const cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 32, 1};
-    if (!encode_tiled(&p.tma_o, ap.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_128B, ap.o, 3, dims, strides, box, why))
-      return BI_ERR_CUDA;
-  }
+  p.o = ap.o;
+  p.o_t = ap.o_t;
+  p.o_l = ap.o_l;
   p.L = (int32_t)ap.L;
   p.Tq = (int32_t)ap.Tq;
   p.Tk = (int32_t)ap.Tk;

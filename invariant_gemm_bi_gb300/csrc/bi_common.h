@@ -112,8 +112,9 @@ struct PatchParams {
 struct AttnParams {
   CUtensorMap tma_q;  // q as {D, Tq, L}, box {64, 128, 1}, 128B swizzle
   CUtensorMap tma_k;  // k as {D, Tk, L}, box {64, 128, 1}
-  CUtensorMap tma_v;  // v as {D, Tk, L}, box {64, 64, 1}
-  CUtensorMap tma_o;  // o as {D, Tq, L}, box {128 bytes of D, 32, 1}
+  CUtensorMap tma_v;  // v as {D, Tk, L}, box {64, 32, 1}
+  void* o;            // o[l][t][d] at o + l*o_l + t*o_t + d (fp32 or bf16)
+  int64_t o_t, o_l;
   int32_t L, Tq, Tk, q_tiles, kv_blocks, num_tiles;
   float score_log2;  // scale * log2(e), rounded once to fp32
   int32_t out_f32;
