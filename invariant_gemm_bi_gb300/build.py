@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]
-SOURCES = ["bi_abi.cu", "bi_gemm.cu", "bi_conv.cu", "bi_patch.cu", "bi_softmax.cu", "bi_rows.cu", "bi_attn.cu"]
+SOURCES = ["bi_abi.cu", "bi_gemm.cu", "bi_conv.cu", "bi_patch.cu", "bi_softmax.cu", "bi_rows.cu", "bi_rows_rms.cu",
+           "bi_rows_lsm.cu", "bi_attn.cu"]
 
 
 def _nvcc() -> str:

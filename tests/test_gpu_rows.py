@@ -89,10 +89,10 @@ def check_mean(y, ref, absmean, N, what=""):
     _assert_within(y, ref, bound, what)
 
 
-# shapes spanning every team size (32 threads for N <= 1024, then 64, 128,
-# 256, 512, 1024 threads), rows longer than one register chunk (N > 32768:
-# re-read per pass), ragged tails (N mod 4 != 0), a single element, a single
-# row and odd row counts (teams of a block left without a row)
+# shapes spanning every team size (32 threads for N <= 1024, 256 for N <=
+# 8192, 1024 beyond), rows longer than one register chunk (N > 32768: re-read
+# per pass), ragged tails (N mod 4 != 0), a single element, a single row and
+# odd row counts (warp teams of a block left without a row)
 SHAPES = [(1, 1), (3, 7), (37, 1000), (11, 2000), (9, 3001), (19, 4099), (9, 8192), (3, 12345),
           (2, 40003), (3, 70001)]
 
