@@ -131,6 +131,7 @@ struct RowParams {
   int64_t R, N, ld_x, ld_y, w_stride;
   int32_t x_kind, y_kind, w_kind;  // 0 bf16, 1 fp16, 2 fp32
   int32_t x_esz, y_esz;            // element sizes in bytes
+  int32_t cl;                      // CTAs per row (a cluster) for 1024-thread teams, else 1
   float eps;
 };
 

@@ -11,12 +11,16 @@
 // G = 16 groups for 16-bit inputs and 8 for fp32, so a thread holds at most G
 // groups of 4 elements (32 registers of data) unless the row is longer than
 // 4096 G elements -- then each of the 1024 threads walks several chunks of G
-// groups.  Teams smaller than 256 threads share a 256-thread block.  The row
-// is cut into groups of 4 consecutive elements; thread t owns groups t, t+T,
-// t+2T, ... and accumulates their elements in
+// groups.  Teams smaller than 256 threads share a 256-thread block.  Rows
+// longer than 4096 G elements are split, by N alone, over a cluster of
+// cl = ceil(N / 4096 G) <= 8 CTAs of 1024 threads: CTA r takes the r-th of
+// cl equal contiguous slices of the row's groups.  The row (or each CTA's
+// slice) is cut into groups of 4 consecutive elements; thread t owns groups
+// t, t+T, t+2T, ... of it and accumulates their elements in
 // ascending index order in fp32; each warp combines its 32 partials by a fixed
-// xor butterfly, and a team of several warps adds the warp partials in warp
-// order.  The order depends only on N, the input type and the element index
+// xor butterfly, a team of several warps adds the warp partials in warp
+// order, and a cluster adds its CTAs' totals in rank order (read by every
+// CTA through distributed shared memory).  The order depends only on N, the input type and the element index
 // -- not on the number of rows, on the row's address (aligned rows are loaded
 // 4 elements at a time, others one at a time, with the same arithmetic) or on
 // which SM runs it.  A thread loads a chunk of G groups, all before using any,
@@ -39,6 +43,7 @@
 
 #include "bi_common.h"
 #include "bi_launch.h"
+#include "bi_ptx.cuh"
 
 namespace bi {
 
@@ -137,27 +142,48 @@ __device__ __forceinline__ bool aligned4(const void* p, int esz) {
   return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)(4 * esz)) == 0;
 }
 
+// The groups [gbeg, gend) of a row that one CTA reduces: the whole row, or
+// for a cluster of cl CTAs the rank-th of cl equal contiguous slices.
+struct RowSpan {
+  int gbeg, gend;
+};
+__device__ __forceinline__ RowSpan row_span(int N, int cl, int rank) {
+  const int ng = (N + 3) >> 2;
+  const int per = (ng + cl - 1) / cl;
+  const int b = min(ng, rank * per);
+  return {b, min(ng, b + per)};
+}
+
 // One chunk of a thread's groups: chunk c holds its groups g0 + k T,
-// k = 0..G-1, g0 = GcT + t, as raw words (zeros past the end of the row).  All loads are
-// issued before any value is used.  `full`: all G groups lie inside the
-// row and were loaded as vectors (no per-element checks needed).
+// k = 0..G-1, g0 = gbeg + GcT + t, as raw words (zeros past the end of the
+// span).  All loads are issued before any value is used.  `full`: all G
+// groups lie inside the span and the row and were loaded as vectors (no
+// per-element checks needed).
 template <int X>
 struct RowChunk {
   static constexpr int G = chunk_groups<X>();
   uint32_t w[G][Elem<X>::kWords];
-  int g0;
+  int g0, gend;
   bool full;
 };
 
-template <int T, int X>
-__device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, int t, int c, RowChunk<X>& ch) {
-  constexpr int W = Elem<X>::kWords;
+// Elements of group g of the row that the span holds (0 outside it).
+__device__ __forceinline__ int group_n(int g, int gend, int N) {
   const int nfull = N >> 2;
-  ch.g0 = c * RowChunk<X>::G * T + t;
-  ch.full = vec && ch.g0 + (RowChunk<X>::G - 1) * T < nfull;
+  return g >= gend ? 0 : (g < nfull ? 4 : (g == nfull ? (N & 3) : 0));
+}
+
+template <int T, int X>
+__device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, const RowSpan& sp, int t, int c,
+                                           RowChunk<X>& ch) {
+  constexpr int W = Elem<X>::kWords;
+  constexpr int G = RowChunk<X>::G;
+  ch.g0 = sp.gbeg + c * G * T + t;
+  ch.gend = sp.gend;
+  ch.full = vec && ch.g0 + (G - 1) * T < min(N >> 2, sp.gend);
   if (ch.full) {
 #pragma unroll
-    for (int k = 0; k < RowChunk<X>::G; ++k) {
+    for (int k = 0; k < G; ++k) {
       const int g = ch.g0 + k * T;
       if constexpr (W == 4) {
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + g);
@@ -170,9 +196,9 @@ __device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, int t
     return;
   }
 #pragma unroll
-  for (int k = 0; k < RowChunk<X>::G; ++k) {
+  for (int k = 0; k < G; ++k) {
     const int g = ch.g0 + k * T;
-    const int n = g < nfull ? 4 : (g == nfull ? (N & 3) : 0);
+    const int n = group_n(g, sp.gend, N);
     if (n == 4 && vec) {
       if constexpr (W == 4) {
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + g);
@@ -195,13 +221,10 @@ __device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, int t
   }
 }
 
-// Elements of group k of the chunk that lie inside the row (0 past its end).
+// Elements of group k of the chunk that lie inside the span (0 past its end).
 template <int T, int X>
 __device__ __forceinline__ int chunk_n(const RowChunk<X>& ch, int k, int N) {
-  if (ch.full) return 4;
-  const int g = ch.g0 + k * T;
-  const int nfull = N >> 2;
-  return g < nfull ? 4 : (g == nfull ? (N & 3) : 0);
+  return ch.full ? 4 : group_n(ch.g0 + k * T, ch.gend, N);
 }
 
 // f(value) over the chunk's elements, groups then elements ascending.
@@ -223,12 +246,57 @@ __device__ __forceinline__ void chunk_visit(const RowChunk<X>& ch, int N, F&& f)
   }
 }
 
-// Chunks a thread of a T-team walks for a row of N elements.
+// Chunks a thread of a T-team walks over a span.
 template <int T, int X>
-__device__ __forceinline__ int row_chunks(int N) {
+__device__ __forceinline__ int row_chunks(const RowSpan& sp) {
   constexpr int G = RowChunk<X>::G;
-  const int groups = (N + 3) >> 2;
-  return (groups + T * G - 1) / (T * G);
+  const int groups = sp.gend - sp.gbeg;
+  return groups <= 0 ? 0 : (groups + T * G - 1) / (T * G);
+}
+
+// Where a thread's team works: its row, its index in the team and the span of
+// the row its CTA reduces (T == 1024 with p.cl > 1: one row per cluster).
+template <int T>
+struct RowSlot {
+  int64_t row;
+  int t;
+  int cl;
+  RowSpan span;
+};
+template <int T>
+__device__ __forceinline__ RowSlot<T> row_slot(const RowParams& p) {
+  RowSlot<T> s;
+  if constexpr (T == 1024) {
+    s.cl = p.cl;
+    s.row = blockIdx.x / s.cl;
+    s.t = threadIdx.x;
+    s.span = row_span((int)p.N, s.cl, (int)(blockIdx.x % s.cl));
+  } else {
+    s.cl = 1;
+    s.row = (int64_t)blockIdx.x * Team<T>::kRows + threadIdx.x / T;
+    s.t = threadIdx.x % T;
+    s.span = row_span((int)p.N, 1, 0);
+  }
+  return s;
+}
+
+// The CTA's total v (the same in every thread) combined over the row's
+// cluster of cl CTAs: each CTA publishes it, the cluster meets at a barrier,
+// and every thread reads the totals of CTAs 0 .. cl-1 in rank order.  cx: two
+// slots, used alternately (a slot is rewritten only after the next barrier,
+// which every reader of it has passed).
+template <bool MAX>
+__device__ __forceinline__ float cluster_combine(float v, float* cx, int cl, int& slot) {
+  if (threadIdx.x == 0) cx[slot] = v;
+  cluster_sync_all();
+  const uint32_t a = smem_u32(cx + slot);
+  float s = ld_shared_cluster_f32(cluster_map_shared(a, 0));
+  for (int r = 1; r < cl; ++r) {
+    const float o = ld_shared_cluster_f32(cluster_map_shared(a, (uint32_t)r));
+    s = MAX ? fmaxf(s, o) : __fadd_rn(s, o);
+  }
+  slot ^= 1;
+  return s;
 }
 
 // Stores the n (<= 4) values of the group starting at element j of a row of
@@ -288,6 +356,33 @@ template <int W>
 __device__ __forceinline__ void load_w4(const RowParams& p, int j, int n, bool wvec, float (&w)[4]) {
   load_w4_kind(p, W == kKindRuntime ? p.w_kind : W, j, n, wvec, w);
 }
+
+// Launches a row kernel, as clusters of rp.cl CTAs when rp.cl > 1.
+template <typename K>
+inline void launch_row_kernel(K kernel, const RowParams& rp, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream) {
+  if (rp.cl > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {};
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)rp.cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, rp);
+  } else {
+    kernel<<<grid, block, smem, stream>>>(rp);
+  }
+}
+
+// CTAs per row: 1, or for rows longer than 4096 G elements ceil(N / 4096 G),
+// at most 8 -- a function of N and the input type only.
+int row_cluster_size(int64_t N, int x_kind);
 
 // Launchers of the three operations for team size T (bi_rows_rms.cu,
 // bi_rows_lsm.cu, bi_rows.cu); grid: one block per Team<T>::kRows rows.

@@ -8,8 +8,10 @@ namespace bi {
 template <int T, int X, int Y>
 __global__ void __launch_bounds__(Team<T>::kBlock, 1024 / Team<T>::kBlock) log_softmax_kernel(const RowParams p) {
   __shared__ float red[Team<T>::kBlock / 32];
-  const int t = threadIdx.x % T;
-  const int64_t row = (int64_t)blockIdx.x * Team<T>::kRows + threadIdx.x / T;
+  __shared__ float cx[2];
+  const RowSlot<T> rs = row_slot<T>(p);
+  const int t = rs.t;
+  const int64_t row = rs.row;
   const bool live = row < p.R;
   if (T == 32 && !live) return;
   const int64_t r0 = live ? row : 0;
@@ -17,24 +19,28 @@ __global__ void __launch_bounds__(Team<T>::kBlock, 1024 / Team<T>::kBlock) log_s
   void* y = static_cast<char*>(p.y) + r0 * p.ld_y * p.y_esz;
   const int N = (int)p.N;
   const bool xvec = aligned4(x, Elem<X>::kBytes);
-  const int nch = live ? row_chunks<T, X>(N) : 0;
+  const int nch = live ? row_chunks<T, X>(rs.span) : 0;
+  int slot = 0;
   RowChunk<X> ch;
   float m = -INFINITY;
   for (int c = 0; c < nch; ++c) {
-    load_chunk<T, X>(x, xvec, N, t, c, ch);
+    load_chunk<T, X>(x, xvec, N, rs.span, t, c, ch);
     chunk_visit<T, X>(ch, N, [&](float v) { m = fmaxf(m, v); });
   }
   m = team_max<T>(m, red);
+  if (T == 1024 && rs.cl > 1) m = cluster_combine<true>(m, cx, rs.cl, slot);
   float acc = 0.0f;
   for (int c = 0; c < nch; ++c) {
-    if (nch > 1) load_chunk<T, X>(x, xvec, N, t, c, ch);
+    if (nch > 1) load_chunk<T, X>(x, xvec, N, rs.span, t, c, ch);
     chunk_visit<T, X>(ch, N, [&](float v) { acc = __fadd_rn(acc, expf(__fsub_rn(v, m))); });
   }
-  const float lse = logf(team_sum<T>(acc, red));
+  float se = team_sum<T>(acc, red);
+  if (T == 1024 && rs.cl > 1) se = cluster_combine<false>(se, cx, rs.cl, slot);
+  const float lse = logf(se);
   if (!live) return;
   const bool yvec = aligned4(y, p.y_esz);
   for (int c = 0; c < nch; ++c) {
-    if (nch > 1) load_chunk<T, X>(x, xvec, N, t, c, ch);
+    if (nch > 1) load_chunk<T, X>(x, xvec, N, rs.span, t, c, ch);
 #pragma unroll
     for (int k = 0; k < RowChunk<X>::G; ++k) {
       const int n = chunk_n<T, X>(ch, k, N);
@@ -45,15 +51,16 @@ __global__ void __launch_bounds__(Team<T>::kBlock, 1024 / Team<T>::kBlock) log_s
       store4<Y>(p, y, 4 * (ch.g0 + k * T), yvec, n, o);
     }
   }
+  if (T == 1024 && rs.cl > 1) cluster_sync_all();  // no CTA leaves while a peer may read its totals
 }
 
 template <int T, int X>
 static void launch_lsm_x(const RowParams& rp, dim3 grid, cudaStream_t stream) {
   const dim3 block(Team<T>::kBlock);
   if (rp.y_kind == X)
-    log_softmax_kernel<T, X, X><<<grid, block, 0, stream>>>(rp);
+    launch_row_kernel(log_softmax_kernel<T, X, X>, rp, grid, block, 0, stream);
   else
-    log_softmax_kernel<T, X, kKindRuntime><<<grid, block, 0, stream>>>(rp);
+    launch_row_kernel(log_softmax_kernel<T, X, kKindRuntime>, rp, grid, block, 0, stream);
 }
 
 template <int T>

@@ -18,20 +18,23 @@ __global__ void __launch_bounds__(Team<T>::kBlock, Team<T>::kBlock >= 512 ? 1 : 
   constexpr bool kStage = rms_stages_weight<T, W>();
   constexpr int kBlock = Team<T>::kBlock;
   __shared__ float red[kBlock / 32];
+  __shared__ float cx[2];
   extern __shared__ float wsm[];  // the weight as fp32 (kStage)
-  const int t = threadIdx.x % T;
-  const int64_t row = (int64_t)blockIdx.x * Team<T>::kRows + threadIdx.x / T;
+  const RowSlot<T> rs = row_slot<T>(p);
+  const int t = rs.t;
+  const int64_t row = rs.row;
   const bool live = row < p.R;
   const int64_t r0 = live ? row : 0;
   const void* x = static_cast<const char*>(p.x) + r0 * p.ld_x * Elem<X>::kBytes;
   void* y = static_cast<char*>(p.y) + r0 * p.ld_y * p.y_esz;
   const int N = (int)p.N;
   const bool xvec = aligned4(x, Elem<X>::kBytes);
-  const int nch = live ? row_chunks<T, X>(N) : 0;
+  const int nch = live ? row_chunks<T, X>(rs.span) : 0;
+  int slot = 0;
   const int wk = W == kKindRuntime ? p.w_kind : (W < 0 ? 0 : W);
   const bool wvec = W != kNoWeight && p.w_stride == 1 && aligned4(p.w, wk == 2 ? 4 : 2);
   RowChunk<X> ch;
-  if (nch > 0) load_chunk<T, X>(x, xvec, N, t, 0, ch);
+  if (nch > 0) load_chunk<T, X>(x, xvec, N, rs.span, t, 0, ch);
   if constexpr (kStage) {
     if (wvec) {
 #pragma unroll 4
@@ -50,17 +53,18 @@ __global__ void __launch_bounds__(Team<T>::kBlock, Team<T>::kBlock >= 512 ? 1 : 
   if (T == 32 && !live) return;  // warp teams hold no later block barrier
   float acc = 0.0f;
   for (int c = 0; c < nch; ++c) {
-    if (c > 0) load_chunk<T, X>(x, xvec, N, t, c, ch);
+    if (c > 0) load_chunk<T, X>(x, xvec, N, rs.span, t, c, ch);
     chunk_visit<T, X>(ch, N, [&](float v) { acc = __fadd_rn(acc, __fmul_rn(v, v)); });
   }
-  const float ss = team_sum<T>(acc, red);
+  float ss = team_sum<T>(acc, red);
+  if (T == 1024 && rs.cl > 1) ss = cluster_combine<false>(ss, cx, rs.cl, slot);
   if (!live) return;  // past the team's last barrier
   const float ms = __fdiv_rn(ss, (float)N);
   const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
   const bool yvec = aligned4(y, p.y_esz);
   constexpr int kWB = 2;  // weight groups loaded together (unstaged weight)
   for (int c = 0; c < nch; ++c) {
-    if (nch > 1) load_chunk<T, X>(x, xvec, N, t, c, ch);  // one chunk: still in registers
+    if (nch > 1) load_chunk<T, X>(x, xvec, N, rs.span, t, c, ch);  // one chunk: still in registers
 #pragma unroll
     for (int k0 = 0; k0 < RowChunk<X>::G; k0 += kWB) {
       float w[kWB][4];
@@ -96,6 +100,7 @@ __global__ void __launch_bounds__(Team<T>::kBlock, Team<T>::kBlock >= 512 ? 1 : 
       }
     }
   }
+  if (T == 1024 && rs.cl > 1) cluster_sync_all();  // no CTA leaves while a peer may read its total
 }
 
 template <int T, int X, int Y, int W>
@@ -104,7 +109,7 @@ static void launch_rms(const RowParams& rp, dim3 grid, cudaStream_t stream) {
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(reinterpret_cast<const void*>(&rmsnorm_kernel<T, X, Y, W>),
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  rmsnorm_kernel<T, X, Y, W><<<grid, dim3(Team<T>::kBlock), smem, stream>>>(rp);
+  launch_row_kernel(rmsnorm_kernel<T, X, Y, W>, rp, grid, dim3(Team<T>::kBlock), smem, stream);
 }
 
 template <int T, int X>

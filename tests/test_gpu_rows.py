@@ -89,12 +89,13 @@ def check_mean(y, ref, absmean, N, what=""):
     _assert_within(y, ref, bound, what)
 
 
-# shapes spanning every team size (32 threads for N <= 1024, 256 for N <=
-# 8192, 1024 beyond), rows longer than one register chunk (N > 32768: re-read
-# per pass), ragged tails (N mod 4 != 0), a single element, a single row and
-# odd row counts (warp teams of a block left without a row)
+# shapes spanning every team size (32, 64, 256 and 1024 threads), rows split
+# over a cluster of 2, 3 or 8 CTAs (N > 4096 G: 32768 fp32 / 65536 16-bit
+# elements per CTA) including more than one register chunk per thread,
+# ragged tails (N mod 4 != 0), a single element, a single row and odd row
+# counts (teams of a block left without a row)
 SHAPES = [(1, 1), (3, 7), (37, 1000), (11, 2000), (9, 3001), (19, 4099), (9, 8192), (3, 12345),
-          (2, 40003), (3, 70001)]
+          (2, 40003), (3, 70001), (1, 600001)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
