@@ -20,7 +20,7 @@
 //          block (keys 0-63, 64-127), a_r the sum of the half's p with key
 //          index = r mod 4, ascending;  l = l_0 + l_1 at the end
 //   O   += bf16(p) v_j                tcgen05.mma 128 x 256 x 16, keys ascending,
-//                                      fp32 in TMEM
+//                                      P read from TMEM, fp32 O in TMEM
 // and finally o = RN(O * RN(1 / l)), rounded once to the output type.  Every
 // step is a function of the query row, the head's keys and values, Tk and
 // scale only: not of L, Tq, the tile a row falls in or the SM that runs it.
@@ -31,8 +31,12 @@
 // w % 4, one row per thread; warps 2-5 take keys 0-63 of each block and O
 // columns 0-127, warps 6-9 keys 64-127 and O columns 128-255.  The two warps
 // of a quadrant exchange their block maxima through a TMEM column of the S
-// buffer they have consumed, and decide every wait together (a barrier that
-// ANDs their outcomes), so they always take the same path.
+// buffer they have consumed, write their halves of the bf16 P row back into
+// that buffer (keys 64h.. at columns 64h..64h+31), and decide every wait
+// together (a barrier that ANDs their outcomes), so they always take the same
+// path.  The tensor core runs one thread's MMAs in issue order, so S_{j+2}
+// (issued after PV_j) never overwrites P_j before PV_j has read it, and the
+// softmax waits for PV_{j-1} only when it must rescale O.
 // Every wait is bounded; on expiry the kernel records the site, stops all
 // roles, drains what it issued and frees TMEM.
 #include <cuda_bf16.h>
@@ -63,8 +67,8 @@ constexpr float kAttnRescaleLog2 = 8.0f;  // keep a stale maximum while p <= 2^8
 
 struct AttnLayout {
   static constexpr int Q = 0;                                       // 4 x [128 rows x 64 D]
-  static constexpr int P = Q + kAttnBM * kAttnD * 2;                // 2 x [128 rows x 64 keys]
-  static constexpr int STG = P + kAttnBM * kAttnBN * 2;             // stage ring
+  static constexpr int OUT = Q + kAttnBM * kAttnD * 2;              // epilogue staging, 4 KB per warp
+  static constexpr int STG = OUT + kAttnSoftmaxWarps * 4096;        // stage ring
   static constexpr int BARS = STG + kAttnStages * kAttnStageBytes;  // mbarriers
   static constexpr int NBARS = 11 + 2 * kAttnStages;
   static constexpr int XCH = BARS + 8 * NBARS;    // running-sum exchange, 2 x 128 floats
@@ -80,7 +84,6 @@ struct AttnBars {
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return b + 16 + 8 * s; }
   __device__ __forceinline__ uint32_t empty(uint32_t s) const { return b + 16 + 8 * kAttnStages + 8 * s; }
   __device__ __forceinline__ uint32_t s_full(uint32_t i) const { return b + 16 + 16 * kAttnStages + 8 * i; }
-  __device__ __forceinline__ uint32_t s_free(uint32_t i) const { return b + 32 + 16 * kAttnStages + 8 * i; }
   __device__ __forceinline__ uint32_t p_full() const { return b + 48 + 16 * kAttnStages; }
   __device__ __forceinline__ uint32_t pv_done() const { return b + 56 + 16 * kAttnStages; }
   __device__ __forceinline__ uint32_t o_full() const { return b + 64 + 16 * kAttnStages; }
@@ -172,8 +175,8 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
 // MMA issuer (one thread): S_0; then per block j: S_{j+1} (other S buffer),
 // PV_j once the softmax warps have written P_j.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& bars, uint32_t sQ, uint32_t sP,
-                                         uint32_t sS, uint32_t tmem, const WaitCtl& wc) {
+__device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& bars, uint32_t sQ, uint32_t sS,
+                                         uint32_t tmem, const WaitCtl& wc) {
   const uint32_t kIdS = idesc_bf16_f32(kAttnBM, kAttnBN, false);
   const uint32_t kIdO = idesc_bf16_f32(kAttnBM, kAttnD, true);
   uint32_t it = 0, sc = 0, pc = 0;
@@ -182,10 +185,11 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
   auto wait = [&](uint32_t bar, uint32_t par) {
     return mbar_wait_bounded(bar, par, wc.abort, wc.status_word, wc.limit_ns, status_code(6, kSiteMmaFull));
   };
+  // S_j goes to TMEM buffer (block count) % 2; it is free: the softmax warps
+  // consumed S_{j-2} before signalling P_{j-2}, and PV_{j-2} -- the last
+  // reader of the buffer -- was issued before this S_j.
   auto issue_s = [&](int j) -> bool {
-    const uint32_t buf = sc & 1, use = sc >> 1;
-    if (use > 0 && !wait(bars.s_free(buf), (use - 1) & 1)) return false;
-    tc_fence_after_sync();
+    const uint32_t buf = sc & 1;
     const uint32_t d = tmem + buf * kAttnBN;
     for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
       const uint32_t s = it % kAttnStages, r = it / kAttnStages;
@@ -211,6 +215,7 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
     return true;
   };
   auto issue_pv = [&](int j) -> bool {
+    const uint32_t pbuf = tmem + (pc & 1) * kAttnBN;  // P_j: in the TMEM buffer of S_j
     const int nst = attn_v_stages(j, p.Tk);
     for (int vs = 0; vs < nst; ++vs) {  // keys vs * kAttnVKeys.. of the block
       const uint32_t s = it % kAttnStages, r = it / kAttnStages;
@@ -220,9 +225,9 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
 #pragma unroll
       for (int k = 0; k < kAttnVKeys / 16; ++k) {  // K = 16 steps over keys, ascending
         const int key = vs * kAttnVKeys + 16 * k;  // first key of the step within the block
-        const uint64_t ad = smem_desc_sw128(sP + (key >> 6) * 16384 + ((key & 63) >> 4) * 32, 16, 1024);
+        const uint32_t acol = pbuf + (key >> 6) * 64 + ((key & 63) >> 4) * 8;
         const uint64_t bd = smem_desc_sw128(vb + k * 2048, kAttnVKeys * 128, 1024);
-        umma_bf16(tmem + kAttnOCol, ad, bd, kIdO, (j | vs | k) != 0 ? 1u : 0u);
+        umma_bf16_ts(tmem + kAttnOCol, acol, bd, kIdO, (j | vs | k) != 0 ? 1u : 0u);
       }
       umma_commit(bars.empty(s));
       ++it;
@@ -255,7 +260,7 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
 // Softmax and epilogue (warps 2-9): one query row and one half of the keys /
 // of O's columns per thread.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars& bars, uint32_t sP,
+__device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars& bars, uint32_t sOut,
                                              float* xch, uint32_t tmem, int warp, int lane, const WaitCtl& wc) {
   const int qd = warp & 3;         // TMEM lane quadrant this warp may access
   const int hc = (warp - 2) >> 2;  // half: keys 64hc.. of a block, O columns 128hc..
@@ -312,17 +317,14 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         for (int i = 8; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], t[i]);
         mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       }
-      // Exchange the halves' maxima through the first column of each half of
-      // the consumed S buffer, then release the buffer.
-      tmem_store_1col(scol, __float_as_uint(mx));
+      // Exchange the halves' maxima through the last column of each half of
+      // the consumed S buffer (P takes the first 32 columns of each half).
+      tmem_store_1col(scol + 63, __float_as_uint(mx));
       tmem_store_wait();
       tc_fence_before_sync();
       named_barrier(pair_bar, 64);
       tc_fence_after_sync();
-      const float mo = __uint_as_float(tmem_load_1col(trow + buf * kAttnBN + (1 - hc) * 64));
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.s_free(buf));
+      const float mo = __uint_as_float(tmem_load_1col(trow + buf * kAttnBN + (1 - hc) * 64 + 63));
       ++sc;
       const float m_blk = hc == 0 ? fmaxf(mx, mo) : fmaxf(mo, mx);  // the same operands in both warps
       const float m_new = fmaxf(m, m_blk);
@@ -348,13 +350,15 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
       const float ps = __fadd_rn(__fadd_rn(a4[0], a4[1]), __fadd_rn(a4[2], a4[3]));
       lsum = __fadd_rn(resc ? __fmul_rn(lsum, alpha) : lsum, ps);
       m = m_use;
-      // PV_{j-1} has finished: P may be overwritten and O is stable.
-      if (pc > 0 && !wait_pair(bars.pv_done(), (pc - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
+      // Rescaling O needs PV_{j-1} finished (O stable).  At most that one PV
+      // can be pending: S_j, whose completion was waited for above, was
+      // issued after PV_{j-2}.
       if (__any_sync(0xffffffffu, resc)) {
+        if (!wait_pair(bars.pv_done(), (pc - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
         const float f = resc ? alpha : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -368,14 +372,19 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         }
         tmem_store_wait();
       }
-      // This half's P row into shared memory: K-major, 128-byte swizzle
-      // (16-byte unit u of row r stored at unit u ^ (r & 7)).
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(sP + hc * 16384 + row * 128 + ((u ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                     pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
+      // This half's P row (64 keys, bf16 pairs) into columns 64 hc .. 64 hc + 31
+      // of the S buffer: the A operand of PV_j.  (The buffer's previous P was
+      // read by PV_{j-2}, complete since S_j, issued after it, is.)
+      tmem_store_32cols(scol, pk);
+      tmem_store_wait();
       tc_fence_before_sync();
+      // Signal P_j only once every warp has signalled P_{j-1}: a warp that ran
+      // ahead (quadrants with no output rows skip the epilogue) must not
+      // arrive twice on one phase.
+      if (pc > 0 && !wait_pair(bars.p_full(), (pc - 1) & 1)) {
+        ok = false;
+        break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.p_full());
       ++pc;
@@ -383,9 +392,9 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     if (!ok) break;
 
     // Epilogue: o = RN(O * RN(1 / (l_0 + l_1))).  Each warp turns its 32 rows
-    // x 128 columns around through its own 4 KB of the P buffer (every PV of
-    // the tile has completed), 128 bytes of each row at a time, so that each
-    // global store instruction writes four whole 128-byte row segments.
+    // x 128 columns around through its own 4 KB of the staging buffer, 128
+    // bytes of each row at a time, so that each global store instruction
+    // writes four whole 128-byte row segments.
     if (!wait_pair(bars.o_full(), local & 1)) {
       ok = false;
       break;
@@ -397,7 +406,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     named_barrier(pair_bar, 64);  // both read before the next tile writes again
     const float rinv = __frcp_rn(hc == 0 ? __fadd_rn(lsum, lo) : __fadd_rn(lo, lsum));
     if (q0 + qd * 32 < p.Tq) {  // warp-uniform: some of its rows are outputs
-      const uint32_t region = sP + hc * 16384 + qd * 4096;
+      const uint32_t region = sOut + (hc * 4 + qd) * 4096;
       const int esz = p.out_f32 ? 4 : 2;
       const int cols = 128 / esz;  // columns per 128-byte piece of a row
       char* obase = static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)(q0 + qd * 32) * p.o_t) * esz;
@@ -452,7 +461,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base + AttnLayout::Q;
-  const uint32_t sP = base + AttnLayout::P;
+  const uint32_t sOut = base + AttnLayout::OUT;
   const uint32_t sS = base + AttnLayout::STG;
   const AttnBars bars{base + AttnLayout::BARS};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnLayout::SLOT);
@@ -467,10 +476,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.s_full(i), 1);
-      mbar_init(bars.s_free(i), kAttnSoftmaxWarps);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(bars.s_full(i), 1);
     mbar_init(bars.p_full(), kAttnSoftmaxWarps);
     mbar_init(bars.pv_done(), 1);
     mbar_init(bars.o_full(), 1);
@@ -495,9 +501,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (warp == 0) {
     if (lane == 0) attn_producer(p, bars, sQ, sS, wc);
   } else if (warp == 1) {
-    if (lane == 0) attn_mma(p, bars, sQ, sP, sS, tmem, wc);
+    if (lane == 0) attn_mma(p, bars, sQ, sS, tmem, wc);
   } else {
-    attn_softmax(p, bars, sP, reinterpret_cast<float*>(smem + AttnLayout::XCH), tmem, warp, lane, wc);
+    attn_softmax(p, bars, sOut, reinterpret_cast<float*>(smem + AttnLayout::XCH), tmem, warp, lane, wc);
   }
 
   tc_fence_before_sync();

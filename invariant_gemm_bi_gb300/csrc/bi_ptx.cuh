@@ -304,6 +304,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M rows in TMEM lanes, two
+// 16-bit elements of K per 32-bit column, K = 16 in 8 columns from a_tmem).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // CTA pair: D rows 0..127 in this CTA's TMEM from its A stage, rows 128..255
 // in the peer's TMEM from the peer's A stage; the N columns of B are split
 // between the two CTAs' B stages (first half here, second half in the peer),

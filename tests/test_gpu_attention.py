@@ -139,6 +139,20 @@ def test_attention_strided_inputs_and_output():
     assert bool((big[:, :, :32] == 7.0).all()) and bool((big[:, :, 32 + D:] == 7.0).all())
 
 
+def test_attention_every_head_of_the_workload_equals_the_head_alone():
+    # B = 32: every CTA runs about twelve tiles, including tiles whose last
+    # row quadrants hold no output rows (816 = 6 x 128 + 48); each head of
+    # the batched run must give the bits of the same head run alone, where
+    # every CTA runs one tile
+    q, k, v = inputs.attention(32)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    o = binding.bi_attention(qg, kg, vg, 1.0 / 16)
+    assert bool(torch.isfinite(o).all())
+    for h in range(0, 256, 5):
+        assert bits_equal(binding.bi_attention(qg[h:h + 1], kg[h:h + 1], vg[h:h + 1], 1.0 / 16), o[h:h + 1]), h
+    assert bits_equal(binding.bi_attention(qg, kg, vg, 1.0 / 16), o)
+
+
 def test_attention_workload_sampled_heads():
     # the timed shape at B = 32: Q, K, V [256, 816, 256]; heads 0, 100 and 255
     # against the oracle, head 0 bit-equal to the B = 1 run
