@@ -439,6 +439,34 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
                                 "roofline_frac": round(b2 / (peaks["hbm_gbs"] * 1e9) / t2, 3), "bound": "hbm"},
                     "pv": point(f1, b3, t3), "cublas_qk_us": round(tcb * 1e6, 2)})
         del s, p, o
+    # a long key range: one sample (8 heads), T = 8192 -- fused with four fixed
+    # 2048-key splits and a merge, the materialised chain, and PyTorch's SDPA
+    ql, kl, vl = inputs.attention(1, t=8192, device="cuda")
+    Lh, T = ql.shape[0], ql.shape[1]
+    fl = 4.0 * Lh * T * T * 256
+    bl = Lh * (3 * 2.0 * T * 256 + 4.0 * T * 256)
+    ol = torch.empty(Lh, T, 256, dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.bi_attention_workspace_bytes(Lh, T, T), dtype=torch.uint8, device="cuda")
+    tfl = measure(lambda: binding.bi_attention_ws(ql, kl, vl, 1.0 / 16, out=ol, workspace=ws), flush_buf, stream,
+                  reps)
+    sl = torch.empty(Lh, T, T, dtype=torch.float32, device="cuda")
+    pl = torch.empty(Lh, T, T, dtype=torch.bfloat16, device="cuda")
+    oc = torch.empty(Lh, T, 256, dtype=torch.float32, device="cuda")
+
+    def chain():
+        binding.bi_bmm(ql, kl.transpose(1, 2), alpha=1.0 / 16, out=sl)
+        binding.bi_softmax_lastdim(sl.view(-1, T), out=pl.view(-1, T))
+        binding.bi_bmm(pl, vl, out=oc)
+    tch = measure(chain, flush_buf, stream, reps)
+    del sl, pl
+    tsd = measure(lambda: torch.nn.functional.scaled_dot_product_attention(ql, kl, vl, scale=1.0 / 16),
+                  flush_buf, stream, reps)
+    long_pt = {"heads": Lh, "T": T, "splits": (T + 2047) // 2048, "fused": point(fl, bl, tfl),
+               "chain_us": round(tch * 1e6, 2), "sdpa_us_bf16_out": round(tsd * 1e6, 2),
+               "fused_head0_equals_head_alone": bits_equal(
+                   binding.bi_attention_ws(ql[:1], kl[:1], vl[:1], 1.0 / 16), ol[:1])}
+    del ql, kl, vl, ol, oc, ws
+    out["attention_long"] = long_pt
     out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0),
                         "fused_head0_bit_equal_all_B": all(bits_equal(of0[B], of0[1]) for B in of0),
                         "sdpa_head0_bit_equal_all_B": all(bits_equal(sd0[B], sd0[1]) for B in sd0)}

@@ -214,6 +214,34 @@ bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* 
                        const bi_tensor* o, bi_stream stream);
 
 /*
+ * Long key ranges.  When Tk > 2048 the key range is split into fixed
+ * 2048-key pieces ("ai-infra handbook: deterministic inference", section on
+ * fixed splitting: a split by a fixed length, never by load, keeps attention
+ * batch-invariant -- the split depends on Tk only).  Each (head, 128 query
+ * rows, split) is one work unit of the kernel above, which writes its partial
+ * O (relative to its own running maximum m_s) and (m_s, l_s) to a workspace;
+ * a merge kernel then forms, per row, M = max_s m_s, w_s = 2^(m_s - M),
+ * l = sum_s RN(w_s l_s), O = sum_s RN(w_s O_s) (splits in ascending order)
+ * and o = RN(O * RN(1 / l)).  Tk <= 2048 is not split and needs no
+ * workspace; bi_attention refuses a longer key range (BI_ERR_INVALID_ARG).
+ *
+ * Bytes of workspace bi_attention_ws needs for [L, Tq] queries against Tk
+ * keys: 0 when Tk <= 2048, else ceil(Tk / 2048) * L * Tq * 258 * 4.
+ */
+int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk);
+
+/*
+ * bi_attention with a caller-owned device workspace (16-byte aligned, at
+ * least bi_attention_workspace_bytes(L, Tq, Tk) bytes; may be NULL when that
+ * is 0).  The workspace is scratch: its contents on entry do not matter and
+ * on return are unspecified; it must not be used by other work on the device
+ * while the call's kernels run (stream order).  Results for Tk <= 2048 are
+ * those of bi_attention, bit for bit.
+ */
+bi_status bi_attention_ws(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                          const bi_tensor* o, void* workspace, int64_t workspace_bytes, bi_stream stream);
+
+/*
  * Row reductions over the last dimension -- the normalisation, log-softmax
  * and mean operations that "Unmasking the True Culprit: Why Temperature=0
  * Doesn't Mean Deterministic LLM Inference" (section "Beyond Matrix

@@ -27,6 +27,7 @@ BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
             "bi_rmsnorm_lastdim", "bi_log_softmax_lastdim", "bi_mean_lastdim", "bi_attention",
+            "bi_attention_workspace_bytes", "bi_attention_ws",
             "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
             "bi_conv_packed_weight_bytes", "bi_conv_pack_weight", "bi_conv2d_patch_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
@@ -115,6 +116,9 @@ def load(path: str | None = None):
                 "bi_log_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_mean_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_attention": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
+                "bi_attention_workspace_bytes": ([ctypes.c_int64] * 3, ctypes.c_int64),
+                "bi_attention_ws": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p, ctypes.c_int64,
+                                     ctypes.c_void_p], st),
                 "bi_packed_weight_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
                 "bi_pack_weight": ([ptr, ctypes.c_void_p, ctypes.c_int64,
                                     ctypes.POINTER(BiPackedWeightDesc), ctypes.c_void_p], st),
@@ -296,6 +300,31 @@ def bi_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out")
     _check(lib, "bi_attention",
            lib.bi_attention(_ref(dq), _ref(dk), _ref(dv), ctypes.c_float(scale), _ref(do), _stream(stream)))
+    return out
+
+
+def bi_attention_workspace_bytes(L: int, Tq: int, Tk: int) -> int:
+    return int(load().bi_attention_workspace_bytes(int(L), int(Tq), int(Tk)))
+
+
+def bi_attention_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+                    out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Fused attention for any key range: for Tk > 2048 a workspace of
+    bi_attention_workspace_bytes(L, Tq, Tk) bytes is used (allocated here when
+    not given)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=out_dtype, device=q.device)
+    need = bi_attention_workspace_bytes(q.shape[0], q.shape[1], k.shape[1])
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None else None)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out")
+    _check(lib, "bi_attention_ws",
+           lib.bi_attention_ws(_ref(dq), _ref(dk), _ref(dv), ctypes.c_float(scale), _ref(do), wptr,
+                               ctypes.c_int64(wbytes), _stream(stream)))
     return out
 
 

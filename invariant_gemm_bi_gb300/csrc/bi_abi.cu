@@ -787,8 +787,10 @@ extern "C" bi_status bi_mean_lastdim(const bi_tensor* x, const bi_tensor* y, bi_
 // ---------------------------------------------------------------------------
 // Fused attention
 // ---------------------------------------------------------------------------
-extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
-                                  const bi_tensor* o, bi_stream stream) {
+namespace {
+
+bi_status attention_impl(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                         const bi_tensor* o, void* ws, int64_t ws_bytes, bi_stream stream) {
   std::string why;
   bi_status st;
   if ((st = check_tensor(q, "q", 3, &why)) != BI_OK) return finish(st, why);
@@ -834,8 +836,34 @@ extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const 
   ap.out_f32 = o->dtype == BI_F32;
   ap.scale = scale;
   ap.L = L, ap.Tq = Tq, ap.Tk = Tk, ap.D = D;
+  ap.ws = ws;
+  ap.ws_bytes = ws_bytes;
+  if (ws && !aligned(ws, 16)) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "the workspace must be 16-byte aligned");
+  if (attention_splits(Tk) > 1 && (!ws || ws_bytes < attention_workspace_bytes(L, Tq, Tk)))
+    return finish(BI_ERR_INVALID_ARG, "a key range longer than 2048 needs a workspace of " +
+                                          std::to_string(attention_workspace_bytes(L, Tq, Tk)) +
+                                          " bytes (bi_attention_workspace_bytes)");
   st = launch_attention(ap, (cudaStream_t)stream, &why);
   return finish(st, why);
+}
+
+}  // namespace
+
+extern "C" int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk) {
+  if (L <= 0 || Tq <= 0 || Tk <= 0) return 0;
+  return attention_workspace_bytes(L, Tq, Tk);
+}
+
+extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                                  const bi_tensor* o, bi_stream stream) {
+  return attention_impl(q, k, v, scale, o, nullptr, 0, stream);
+}
+
+extern "C" bi_status bi_attention_ws(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                                     const bi_tensor* o, void* workspace, int64_t workspace_bytes,
+                                     bi_stream stream) {
+  if (workspace_bytes < 0) return finish(BI_ERR_INVALID_ARG, "negative workspace size");
+  return attention_impl(q, k, v, scale, o, workspace, workspace_bytes, stream);
 }
 
 extern "C" bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream stream) {
@@ -914,4 +942,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 6; }
+extern "C" int32_t bi_abi_version(void) { return 7; }

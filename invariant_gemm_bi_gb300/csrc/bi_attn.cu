@@ -64,6 +64,7 @@ constexpr int kAttnSoftmaxWarps = 8;
 constexpr uint32_t kAttnTmemCols = 512;  // S buffers at columns 0 and 128, O at 256
 constexpr uint32_t kAttnOCol = 256;
 constexpr float kAttnRescaleLog2 = 8.0f;  // keep a stale maximum while p <= 2^8
+constexpr int kAttnSplitKeys = 2048;       // key range of one split (a multiple of kAttnBN)
 
 struct AttnLayout {
   static constexpr int Q = 0;                                       // 4 x [128 rows x 64 D]
@@ -104,6 +105,26 @@ __device__ __forceinline__ int attn_v_stages(int j, int Tk) {
   return left >= kAttnBN ? kAttnBN / kAttnVKeys : (left + kAttnVKeys - 1) / kAttnVKeys;
 }
 
+// A work unit: head l, query rows q0 .. q0+127, and keys k0 .. k0+tk-1 (split
+// sp of the key range; the whole range when it is not split) in nkb blocks.
+// Units of one head and split are adjacent so that the CTAs working on them at
+// the same time share its K and V in L2.
+struct AttnTile {
+  int l, q0, sp, k0, tk, nkb;
+};
+__device__ __forceinline__ AttnTile attn_tile(const AttnParams& p, int tile) {
+  AttnTile t;
+  const int per_head = p.ns * p.q_tiles;
+  t.l = tile / per_head;
+  const int r = tile - t.l * per_head;
+  t.sp = r / p.q_tiles;
+  t.q0 = (r - t.sp * p.q_tiles) * kAttnBM;
+  t.k0 = t.sp * kAttnSplitKeys;
+  t.tk = min(p.Tk - t.k0, kAttnSplitKeys);
+  t.nkb = (t.tk + kAttnBN - 1) / kAttnBN;
+  return t;
+}
+
 // ---------------------------------------------------------------------------
 // Producer (one thread): per tile the q tile, then K_0, and for each block j
 // K_{j+1} (if any) followed by V_j -- the order the MMA issuer consumes them.
@@ -124,28 +145,30 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
     ++it;
     return true;
   };
-  auto load_k = [&](int j, int l) -> bool {  // all keys of block j, D columns 64c.. per piece
+  auto load_k = [&](int j, const AttnTile& t) -> bool {  // all keys of block j, D columns 64c.. per piece
     for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
       for (int b = 0; b < kAttnKC; ++b)
-        tma_load_3d(dst + b * 16384, &p.tma_k, bar, (cs * kAttnKC + b) * 64, j * kAttnBN, l);
+        tma_load_3d(dst + b * 16384, &p.tma_k, bar, (cs * kAttnKC + b) * 64, t.k0 + j * kAttnBN, t.l);
     }
     return true;
   };
-  auto load_v = [&](int j, int l) -> bool {  // kAttnVKeys keys of block j per stage, all D
-    const int nst = attn_v_stages(j, p.Tk);
+  auto load_v = [&](int j, const AttnTile& t) -> bool {  // kAttnVKeys keys of block j per stage, all D
+    const int nst = attn_v_stages(j, t.tk);
     for (int vs = 0; vs < nst; ++vs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
       for (int c = 0; c < 4; ++c)
-        tma_load_3d(dst + c * (kAttnVKeys * 128), &p.tma_v, bar, c * 64, j * kAttnBN + vs * kAttnVKeys, l);
+        tma_load_3d(dst + c * (kAttnVKeys * 128), &p.tma_v, bar, c * 64, t.k0 + j * kAttnBN + vs * kAttnVKeys,
+                    t.l);
     }
     return true;
   };
   for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-    const int l = tile / p.q_tiles;
-    const int q0 = (tile - l * p.q_tiles) * kAttnBM;
+    const AttnTile t = attn_tile(p, tile);
+    const int l = t.l;
+    const int q0 = t.q0;
     if (q_loads > 0 && !mbar_wait_bounded(bars.q_empty(), (q_loads - 1) & 1, wc.abort, wc.status_word,
                                           wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
       ok = false;
@@ -154,10 +177,10 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
     mbar_arrive_expect_tx(bars.q_full(), kAttnBM * kAttnD * 2);
     for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * 16384, &p.tma_q, bars.q_full(), c * 64, q0, l);
     ++q_loads;
-    ok = load_k(0, l);
-    for (int j = 0; ok && j < p.kv_blocks; ++j) {
-      if (j + 1 < p.kv_blocks) ok = load_k(j + 1, l);
-      if (ok) ok = load_v(j, l);
+    ok = load_k(0, t);
+    for (int j = 0; ok && j < t.nkb; ++j) {
+      if (j + 1 < t.nkb) ok = load_k(j + 1, t);
+      if (ok) ok = load_v(j, t);
     }
   }
   // No copy may still be landing in shared memory when the CTA exits.
@@ -188,6 +211,7 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
   // S_j goes to TMEM buffer (block count) % 2; it is free: the softmax warps
   // consumed S_{j-2} before signalling P_{j-2}, and PV_{j-2} -- the last
   // reader of the buffer -- was issued before this S_j.
+  int nkb = 0, tk = 0;  // the current tile's key blocks and keys
   auto issue_s = [&](int j) -> bool {
     const uint32_t buf = sc & 1;
     const uint32_t d = tmem + buf * kAttnBN;
@@ -211,12 +235,12 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
     }
     umma_commit(bars.s_full(buf));
     ++sc;
-    if (j == p.kv_blocks - 1) umma_commit(bars.q_empty());  // the tile's last read of q
+    if (j == nkb - 1) umma_commit(bars.q_empty());  // the tile's last read of q
     return true;
   };
   auto issue_pv = [&](int j) -> bool {
     const uint32_t pbuf = tmem + (pc & 1) * kAttnBN;  // P_j: in the TMEM buffer of S_j
-    const int nst = attn_v_stages(j, p.Tk);
+    const int nst = attn_v_stages(j, tk);
     for (int vs = 0; vs < nst; ++vs) {  // keys vs * kAttnVKeys.. of the block
       const uint32_t s = it % kAttnStages, r = it / kAttnStages;
       if (!wait(bars.full(s), r & 1)) return false;
@@ -237,11 +261,14 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
     return true;
   };
   for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+    const AttnTile t = attn_tile(p, tile);
+    nkb = t.nkb;
+    tk = t.tk;
     if (!wait(bars.q_full(), local & 1)) break;
     tc_fence_after_sync();
     ok = issue_s(0);
-    for (int j = 0; ok && j < p.kv_blocks; ++j) {
-      if (j + 1 < p.kv_blocks) ok = issue_s(j + 1);
+    for (int j = 0; ok && j < nkb; ++j) {
+      if (j + 1 < nkb) ok = issue_s(j + 1);
       if (ok) ok = wait(bars.p_full(), pc & 1);
       if (ok && j == 0 && local > 0) ok = wait(bars.o_free(), (local - 1) & 1);  // O is overwritten
       if (ok) {
@@ -278,10 +305,11 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
   };
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
-    const int l = tile / p.q_tiles;
-    const int q0 = (tile - l * p.q_tiles) * kAttnBM;
+    const AttnTile tl = attn_tile(p, tile);
+    const int l = tl.l;
+    const int q0 = tl.q0;
     float m = -INFINITY, lsum = 0.0f;
-    for (int j = 0; j < p.kv_blocks; ++j) {
+    for (int j = 0; j < tl.nkb; ++j) {
       const uint32_t buf = sc & 1, use = sc >> 1;
       if (!wait_pair(bars.s_full(buf), use & 1)) {
         ok = false;
@@ -302,7 +330,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
           t[32 + i] = __fmul_rn(__uint_as_float(r1[i]), c2);
         }
       }
-      const int kvalid = p.Tk - j * kAttnBN - hc * 64;  // keys of this half below Tk
+      const int kvalid = tl.tk - j * kAttnBN - hc * 64;  // keys of this half inside the range
       if (kvalid < 64) {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
@@ -404,15 +432,29 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     named_barrier(pair_bar, 64);
     const float lo = xch[(1 - hc) * kAttnBM + row];
     named_barrier(pair_bar, 64);  // both read before the next tile writes again
-    const float rinv = __frcp_rn(hc == 0 ? __fadd_rn(lsum, lo) : __fadd_rn(lo, lsum));
+    const float lrow = hc == 0 ? __fadd_rn(lsum, lo) : __fadd_rn(lo, lsum);
+    // Unsplit key range: the output o = RN(O * RN(1 / l)).  A split writes its
+    // partial O (unnormalised, relative to its running maximum m) and (m, l)
+    // to the workspace for the merge.
+    const bool split = p.ns > 1;
+    const float rinv = split ? 1.0f : __frcp_rn(lrow);
+    if (split && hc == 0 && q0 + row < p.Tq) {
+      float* ml = p.ws_ml + (((int64_t)tl.sp * p.L + l) * p.Tq + q0 + row) * 2;
+      ml[0] = m;
+      ml[1] = lrow;
+    }
     if (q0 + qd * 32 < p.Tq) {  // warp-uniform: some of its rows are outputs
       const uint32_t region = sOut + (hc * 4 + qd) * 4096;
-      const int esz = p.out_f32 ? 4 : 2;
+      const bool f32 = split || p.out_f32;
+      const int esz = f32 ? 4 : 2;
       const int cols = 128 / esz;  // columns per 128-byte piece of a row
-      char* obase = static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)(q0 + qd * 32) * p.o_t) * esz;
+      const int64_t ot = split ? kAttnD : p.o_t;
+      char* obase =
+          split ? reinterpret_cast<char*>(p.ws_o + (((int64_t)tl.sp * p.L + l) * p.Tq + q0 + qd * 32) * kAttnD)
+                : static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)(q0 + qd * 32) * p.o_t) * esz;
       for (int c = 0; c < 128 / cols; ++c) {
         uint32_t w[32];
-        if (p.out_f32) {
+        if (f32) {
           uint32_t r[32];
           tmem_load_32cols(trow + kAttnOCol + hc * 128 + c * 32, r);
           tmem_load_wait(r);
@@ -445,7 +487,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
           const int rr = 4 * i + (lane >> 3);
           const uint4 v = ld_shared_v4(region + rr * 128 + ((u ^ (rr & 7)) << 4));
           if (q0 + qd * 32 + rr < p.Tq)
-            *reinterpret_cast<uint4*>(obase + ((int64_t)rr * p.o_t + col) * esz) = v;
+            *reinterpret_cast<uint4*>(obase + ((int64_t)rr * ot + col) * esz) = v;
         }
       }
     }
@@ -515,6 +557,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// Merge of a split key range, one 256-thread block per (head, query row),
+// thread d for output column d: M = max over splits of m_s (log2 units);
+// w_s = 2^(m_s - M); l = sum_s RN(w_s l_s), O_d = sum_s RN(w_s O_s,d), both in
+// ascending split order; o_d = RN(O_d * RN(1 / l)), rounded once to o's type.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kAttnD) attn_merge_kernel(const AttnParams p) {
+  const int64_t rowi = blockIdx.x;  // l * Tq + q
+  const int l = (int)(rowi / p.Tq);
+  const int q = (int)(rowi - (int64_t)l * p.Tq);
+  const int d = threadIdx.x;
+  const int64_t per_split = (int64_t)p.L * p.Tq;
+  float M = -INFINITY;
+  for (int s = 0; s < p.ns; ++s) M = fmaxf(M, p.ws_ml[(s * per_split + rowi) * 2]);
+  float lsum = 0.0f, o = 0.0f;
+  for (int s = 0; s < p.ns; ++s) {
+    const float w = ex2_approx(__fsub_rn(p.ws_ml[(s * per_split + rowi) * 2], M));
+    const float ls = __fmul_rn(w, p.ws_ml[(s * per_split + rowi) * 2 + 1]);
+    const float os = __fmul_rn(w, p.ws_o[(s * per_split + rowi) * kAttnD + d]);
+    lsum = s == 0 ? ls : __fadd_rn(lsum, ls);
+    o = s == 0 ? os : __fadd_rn(o, os);
+  }
+  const float v = __fmul_rn(o, __frcp_rn(lsum));
+  char* dst = static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)q * p.o_t + d) * (p.out_f32 ? 4 : 2);
+  if (p.out_f32)
+    *reinterpret_cast<float*>(dst) = v;
+  else
+    *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(v);
+}
+
+int64_t attention_splits(int64_t Tk) { return Tk <= kAttnSplitKeys ? 1 : (Tk + kAttnSplitKeys - 1) / kAttnSplitKeys; }
+
+int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk) {
+  const int64_t ns = attention_splits(Tk);
+  return ns == 1 ? 0 : ns * L * Tq * (kAttnD + 2) * (int64_t)sizeof(float);
+}
+
 bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why) {
   DeviceInfo dev;
   bi_status st = current_device_info(&dev, why);
@@ -544,7 +623,18 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   p.Tk = (int32_t)ap.Tk;
   p.q_tiles = (int32_t)((ap.Tq + kAttnBM - 1) / kAttnBM);
   p.kv_blocks = (int32_t)((ap.Tk + kAttnBN - 1) / kAttnBN);
-  const int64_t tiles = ap.L * (int64_t)p.q_tiles;
+  p.ns = (int32_t)attention_splits(ap.Tk);
+  if (p.ns > 1) {
+    const int64_t need = attention_workspace_bytes(ap.L, ap.Tq, ap.Tk);
+    if (!ap.ws || ap.ws_bytes < need) {
+      *why = "a key range longer than " + std::to_string(kAttnSplitKeys) + " needs a workspace of " +
+             std::to_string(need) + " bytes";
+      return BI_ERR_INVALID_ARG;
+    }
+    p.ws_o = static_cast<float*>(ap.ws);
+    p.ws_ml = p.ws_o + p.ns * ap.L * ap.Tq * kAttnD;
+  }
+  const int64_t tiles = ap.L * (int64_t)p.q_tiles * p.ns;
   if (tiles > INT32_MAX) {
     *why = "tile count exceeds 2^31";
     return BI_ERR_INVALID_ARG;
@@ -558,6 +648,14 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   if (e == cudaSuccess) {
     const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
     attn_kernel<<<grid, kAttnThreads, AttnLayout::DYN, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && p.ns > 1) {
+    if (ap.L * ap.Tq > INT32_MAX) {
+      *why = "too many query rows for the split merge";
+      return BI_ERR_INVALID_ARG;
+    }
+    attn_merge_kernel<<<(unsigned)(ap.L * ap.Tq), kAttnD, 0, stream>>>(p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -115,6 +115,9 @@ struct AttnParams {
   CUtensorMap tma_v;  // v as {D, Tk, L}, box {64, 32, 1}
   void* o;            // o[l][t][d] at o + l*o_l + t*o_t + d (fp32 or bf16)
   int64_t o_t, o_l;
+  float* ws_o;        // split key range: partial O [ns][L][Tq][256]
+  float* ws_ml;       // and (m, l) [ns][L][Tq][2]
+  int32_t ns;         // key-range splits (1: not split)
   int32_t L, Tq, Tk, q_tiles, kv_blocks, num_tiles;
   float score_log2;  // scale * log2(e), rounded once to fp32
   int32_t out_f32;

@@ -125,8 +125,13 @@ struct AttnProblem {
   int out_f32;
   float scale;
   int64_t L, Tq, Tk, D;
+  void* ws;  // workspace for a split key range (Tk > 2048), or null
+  int64_t ws_bytes;
 };
 bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why);
+// Key-range splits (2048 keys each) and the workspace they need (0 if one).
+int64_t attention_splits(int64_t Tk);
+int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk);
 
 // op: kRowRmsNorm, kRowLogSoftmax or kRowMean.
 bi_status launch_row_reduction(int op, const RowParams& rp, cudaStream_t stream, std::string* why);

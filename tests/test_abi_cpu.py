@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 6
+    assert lib.bi_abi_version() == 7
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -296,3 +296,27 @@ def test_attention_validation(lib):
     if not torch.cuda.is_available():
         assert call(q, k, v, o) == binding.BI_ERR_NO_DEVICE
         assert call(q, k, v, _t([2, 100, 256], dtype=0)) == binding.BI_ERR_NO_DEVICE
+
+
+def test_attention_workspace_rules(lib):
+    # no workspace up to 2048 keys; ceil(Tk / 2048) splits of L*Tq*(256+2) floats beyond
+    assert lib.bi_attention_workspace_bytes(2, 100, 2048) == 0
+    assert lib.bi_attention_workspace_bytes(2, 100, 2049) == 2 * 2 * 100 * 258 * 4
+    assert lib.bi_attention_workspace_bytes(3, 7, 6145) == 4 * 3 * 7 * 258 * 4
+    assert lib.bi_attention_workspace_bytes(0, 7, 6145) == 0
+    q, k, v, o = _t([2, 100, 256]), _t([2, 3000, 256]), _t([2, 3000, 256]), _t([2, 100, 256], dtype=2)
+    f = ctypes.c_float(0.0625)
+    need = lib.bi_attention_workspace_bytes(2, 100, 3000)
+    # a long key range without (enough) workspace is refused before any launch
+    assert lib.bi_attention(_r(q), _r(k), _r(v), f, _r(o), None) == binding.BI_ERR_INVALID_ARG
+    assert "workspace" in binding.last_error_message()
+    assert lib.bi_attention_ws(_r(q), _r(k), _r(v), f, _r(o), ctypes.c_void_p(FAKE), ctypes.c_int64(need - 1),
+                               None) == binding.BI_ERR_INVALID_ARG
+    assert lib.bi_attention_ws(_r(q), _r(k), _r(v), f, _r(o), ctypes.c_void_p(FAKE + 8), ctypes.c_int64(need),
+                               None) == binding.BI_ERR_UNSUPPORTED_LAYOUT
+    assert lib.bi_attention_ws(_r(q), _r(k), _r(v), f, _r(o), ctypes.c_void_p(FAKE), ctypes.c_int64(-1),
+                               None) == binding.BI_ERR_INVALID_ARG
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.bi_attention_ws(_r(q), _r(k), _r(v), f, _r(o), ctypes.c_void_p(FAKE), ctypes.c_int64(need),
+                                   None) == binding.BI_ERR_NO_DEVICE

@@ -164,3 +164,59 @@ def test_attention_workload_sampled_heads():
         check_attention(o[h:h + 1], ref, absum, smax, 816, f"B=32 head {h}")
     o1 = binding.bi_attention(qg[:8], kg[:8], vg[:8], 1.0 / 16)
     assert bits_equal(o1, o[:8])
+
+
+# ---------------------------------------------------------------------------
+# Key ranges longer than 2048: fixed 2048-key splits merged in split order
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(2, 130, 2049), (1, 300, 4096), (3, 64, 5000), (1, 40, 9000)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_attention_split_key_range_matches_oracle(shape, out_dtype):
+    L, Tq, Tk = shape
+    q, k, v = _qkv(L, Tq, Tk, 60)
+    ref, absum, smax = oracle.attention(q, k, v, 1.0 / 16)
+    o = binding.bi_attention_ws(q.cuda(), k.cuda(), v.cuda(), 1.0 / 16, out_dtype=out_dtype)
+    check_attention(o, ref, absum, smax, Tk, f"split attention {shape} -> {out_dtype}")
+
+
+def test_attention_split_invariances():
+    # heads alone vs in a batch, query chunks, run to run, and a caller-given
+    # workspace full of garbage: all the same bits
+    L, Tq, Tk = 6, 260, 4500
+    q, k, v = _qkv(L, Tq, Tk, 61)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    full = binding.bi_attention_ws(qg, kg, vg, 1.0 / 16)
+    for h in (0, 3, 5):
+        assert bits_equal(binding.bi_attention_ws(qg[h:h + 1], kg[h:h + 1], vg[h:h + 1], 1.0 / 16),
+                          full[h:h + 1]), h
+    for a, b in ((0, 1), (100, 260), (127, 131)):
+        assert bits_equal(binding.bi_attention_ws(qg[:, a:b].contiguous(), kg, vg, 1.0 / 16), full[:, a:b])
+    ws = torch.full((binding.bi_attention_workspace_bytes(L, Tq, Tk),), 0xFF, dtype=torch.uint8, device="cuda")
+    assert bits_equal(binding.bi_attention_ws(qg, kg, vg, 1.0 / 16, workspace=ws), full)
+    ref, absum, smax = oracle.attention(q[:2], k[:2], v[:2], 1.0 / 16)
+    check_attention(full[:2], ref, absum, smax, Tk, "split attention heads 0-1")
+
+
+def test_attention_split_rescales_across_splits():
+    # scores rising along the keys: the maximum moves in every block and the
+    # later splits dominate the merge
+    L, Tq, Tk = 1, 70, 5000
+    q = (torch.ones(L, Tq, D) * 0.25).to(torch.bfloat16)
+    ramp = torch.arange(Tk, dtype=torch.float32) / 40.0
+    k = (ramp[None, :, None] * torch.ones(L, Tk, D)).to(torch.bfloat16)
+    k[:, :, 1::2] *= -0.5
+    v = inputs.normal_bf16((L, Tk, D), 1.0, 62)
+    ref, absum, smax = oracle.attention(q, k, v, 0.1)
+    o = binding.bi_attention_ws(q.cuda(), k.cuda(), v.cuda(), 0.1)
+    check_attention(o, ref, absum, smax, Tk, "split attention, rising scores")
+
+
+def test_attention_unsplit_range_is_the_same_with_or_without_workspace():
+    q, k, v = _qkv(2, 200, 2048, 63)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    assert binding.bi_attention_workspace_bytes(2, 200, 2048) == 0
+    assert bits_equal(binding.bi_attention_ws(qg, kg, vg, 0.0625), binding.bi_attention(qg, kg, vg, 0.0625))
+    with pytest.raises(binding.BiError) as ei:
+        binding.bi_attention(qg, torch.cat([kg, kg[:, :1]], 1), torch.cat([vg, vg[:, :1]], 1), 0.0625)
+    assert ei.value.status == binding.BI_ERR_INVALID_ARG
