@@ -242,6 +242,20 @@ bi_status bi_attention_ws(const bi_tensor* q, const bi_tensor* k, const bi_tenso
                           const bi_tensor* o, void* workspace, int64_t workspace_bytes, bi_stream stream);
 
 /*
+ * bi_attention_ws without a caller workspace: a split key range uses a
+ * scratch area the library keeps in static device memory (64 MiB per device,
+ * 256-byte aligned, allocated when the library's module is loaded on the
+ * device).  A problem whose workspace would not fit returns
+ * BI_ERR_INVALID_ARG before any launch (use bi_attention_ws).  The scratch is
+ * shared by every call on the device, so calls must not overlap: issue them
+ * on one stream or order them.  Results are those of bi_attention_ws, bit
+ * for bit.  The pages have no counterpart of this entry point: it packages
+ * the same operation for callers that cannot allocate device memory.
+ */
+bi_status bi_attention_noalloc(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                               const bi_tensor* o, bi_stream stream);
+
+/*
  * Row reductions over the last dimension -- the normalisation, log-softmax
  * and mean operations that "Unmasking the True Culprit: Why Temperature=0
  * Doesn't Mean Deterministic LLM Inference" (section "Beyond Matrix

@@ -27,7 +27,7 @@ BI_ERR_NO_DEVICE = 7
 
 EXPORTED = ("bi_mm", "bi_addmm", "bi_bmm", "bi_conv2d_patch", "bi_softmax_lastdim",
             "bi_rmsnorm_lastdim", "bi_log_softmax_lastdim", "bi_mean_lastdim", "bi_attention",
-            "bi_attention_workspace_bytes", "bi_attention_ws",
+            "bi_attention_workspace_bytes", "bi_attention_ws", "bi_attention_noalloc",
             "bi_packed_weight_bytes", "bi_pack_weight", "bi_addmm_packed",
             "bi_conv_packed_weight_bytes", "bi_conv_pack_weight", "bi_conv2d_patch_packed",
             "bi_device_status", "bi_debug_expire_wait", "bi_status_string",
@@ -117,6 +117,7 @@ def load(path: str | None = None):
                 "bi_mean_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_attention": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
                 "bi_attention_workspace_bytes": ([ctypes.c_int64] * 3, ctypes.c_int64),
+                "bi_attention_noalloc": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
                 "bi_attention_ws": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p, ctypes.c_int64,
                                      ctypes.c_void_p], st),
                 "bi_packed_weight_bytes": ([ctypes.c_int64, ctypes.c_int64], ctypes.c_int64),
@@ -325,6 +326,20 @@ def bi_attention_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: fl
     _check(lib, "bi_attention_ws",
            lib.bi_attention_ws(_ref(dq), _ref(dk), _ref(dv), ctypes.c_float(scale), _ref(do), wptr,
                                ctypes.c_int64(wbytes), _stream(stream)))
+    return out
+
+
+def bi_attention_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
+                         out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                         stream=None) -> torch.Tensor:
+    """Fused attention for any key range without a workspace argument: long
+    key ranges use the library's static device scratch (64 MiB per device)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=out_dtype, device=q.device)
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out")
+    _check(lib, "bi_attention_noalloc",
+           lib.bi_attention_noalloc(_ref(dq), _ref(dk), _ref(dv), ctypes.c_float(scale), _ref(do), _stream(stream)))
     return out
 
 

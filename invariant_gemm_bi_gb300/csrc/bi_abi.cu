@@ -16,6 +16,12 @@
 // First device-side failure since the last bi_device_status() (0 = none).
 __device__ unsigned int g_bi_status_word;
 
+// Static device scratch of bi_attention_noalloc (each device's context holds
+// its own copy).  Uninitialised: it costs device memory at module load, not
+// space in the library file.
+constexpr int64_t kNoAllocScratchBytes = 64ll << 20;
+__device__ __align__(256) unsigned char g_bi_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace bi {
 
 namespace {
@@ -32,6 +38,7 @@ struct DevState {
   unsigned int* status_word = nullptr;
   bool smem_set[16] = {};
   int pairs[16] = {};  // resident 2-CTA clusters per kernel slot (0: not yet asked)
+  void* scratch = nullptr;  // device address of g_bi_noalloc_scratch (0: not yet asked)
 };
 DevState g_dev[kMaxDevices];
 
@@ -857,6 +864,45 @@ extern "C" int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t T
 extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
                                   const bi_tensor* o, bi_stream stream) {
   return attention_impl(q, k, v, scale, o, nullptr, 0, stream);
+}
+
+// The device address of this device's static scratch (resolved once per device).
+static bi_status noalloc_scratch(void** out, std::string* why) {
+  DeviceInfo dev;
+  bi_status st = current_device_info(&dev, why);
+  if (st != BI_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev.device];
+  if (!d.scratch) {
+    void* addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_bi_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *why = std::string("scratch address: ") + cudaGetErrorString(e);
+      cudaGetLastError();
+      return BI_ERR_CUDA;
+    }
+    d.scratch = addr;
+  }
+  *out = d.scratch;
+  return BI_OK;
+}
+
+extern "C" bi_status bi_attention_noalloc(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
+                                          const bi_tensor* o, bi_stream stream) {
+  std::string why;
+  bi_status st;
+  if ((st = check_tensor(q, "q", 3, &why)) != BI_OK) return finish(st, why);
+  if ((st = check_tensor(k, "k", 3, &why)) != BI_OK) return finish(st, why);
+  const int64_t need = attention_workspace_bytes(q->shape[0], q->shape[1], k->shape[1]);
+  if (q->shape[0] == 0 || q->shape[1] == 0 || k->shape[1] == 0 || need == 0)
+    return attention_impl(q, k, v, scale, o, nullptr, 0, stream);
+  if (need > kNoAllocScratchBytes)
+    return finish(BI_ERR_INVALID_ARG, "the split key range needs " + std::to_string(need) +
+                                          " bytes of scratch, more than the library's static " +
+                                          std::to_string(kNoAllocScratchBytes) + " (use bi_attention_ws)");
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch, &why)) != BI_OK) return finish(st, why);
+  return attention_impl(q, k, v, scale, o, scratch, kNoAllocScratchBytes, stream);
 }
 
 extern "C" bi_status bi_attention_ws(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
