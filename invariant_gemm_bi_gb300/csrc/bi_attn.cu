@@ -43,6 +43,7 @@
 
 #include "bi_common.h"
 #include "bi_launch.h"
+#include "bi_ptx_ext.cuh"
 #include "bi_roles.cuh"
 
 namespace bi {

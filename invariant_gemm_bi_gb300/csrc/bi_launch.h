@@ -14,6 +14,37 @@
 
 namespace bi {
 
+// Fused attention (bi_attn.cu): o[l] = softmax(scale * q[l] k[l]^T) v[l].
+struct AttnParams {
+  CUtensorMap tma_q;  // q as {D, Tq, L}, box {64, 128, 1}, 128B swizzle
+  CUtensorMap tma_k;  // k as {D, Tk, L}, box {64, 128, 1}
+  CUtensorMap tma_v;  // v as {D, Tk, L}, box {64, 32, 1}
+  void* o;            // o[l][t][d] at o + l*o_l + t*o_t + d (fp32 or bf16)
+  int64_t o_t, o_l;
+  float* ws_o;        // split key range: partial O [ns][L][Tq][256]
+  float* ws_ml;       // and (m, l) [ns][L][Tq][2]
+  int32_t ns;         // key-range splits (1: not split)
+  int32_t L, Tq, Tk, q_tiles, kv_blocks, num_tiles;
+  float score_log2;  // scale * log2(e), rounded once to fp32
+  int32_t out_f32;
+  unsigned int* status_word;
+  uint64_t wait_limit_ns;
+};
+
+// Row reductions over the last dimension (see bi_rows.cu).
+enum : int { kRowRmsNorm = 0, kRowLogSoftmax = 1, kRowMean = 2 };
+struct RowParams {
+  const void* x;  // [R][N], row stride ld_x elements, unit column stride
+  void* y;        // [R][N] (row stride ld_y), or for the mean [R] (stride ld_y)
+  const void* w;  // RMSNorm weight [N] (stride w_stride), or null
+  int64_t R, N, ld_x, ld_y, w_stride;
+  int32_t x_kind, y_kind, w_kind;  // 0 bf16, 1 fp16, 2 fp32
+  int32_t x_esz, y_esz;            // element sizes in bytes
+  int32_t cl;                      // CTAs per row (a cluster) for 1024-thread teams, else 1
+  float eps;
+};
+
+
 // Bound on every device-side wait: far above any legitimate wait (a tile's
 // whole K loop takes well under a millisecond), short enough that a broken
 // pipeline returns an error instead of holding the GPU.

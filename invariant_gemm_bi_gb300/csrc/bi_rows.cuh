@@ -43,7 +43,7 @@
 
 #include "bi_common.h"
 #include "bi_launch.h"
-#include "bi_ptx.cuh"
+#include "bi_ptx_ext.cuh"
 
 namespace bi {
 
