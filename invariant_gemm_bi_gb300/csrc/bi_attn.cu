@@ -623,7 +623,6 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   p.Tq = (int32_t)ap.Tq;
   p.Tk = (int32_t)ap.Tk;
   p.q_tiles = (int32_t)((ap.Tq + kAttnBM - 1) / kAttnBM);
-  p.kv_blocks = (int32_t)((ap.Tk + kAttnBN - 1) / kAttnBN);
   p.ns = (int32_t)attention_splits(ap.Tk);
   if (p.ns > 1) {
     const int64_t need = attention_workspace_bytes(ap.L, ap.Tq, ap.Tk);

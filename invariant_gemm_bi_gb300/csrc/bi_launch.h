@@ -24,7 +24,7 @@ struct AttnParams {
   float* ws_o;        // split key range: partial O [ns][L][Tq][256]
   float* ws_ml;       // and (m, l) [ns][L][Tq][2]
   int32_t ns;         // key-range splits (1: not split)
-  int32_t L, Tq, Tk, q_tiles, kv_blocks, num_tiles;
+  int32_t L, Tq, Tk, q_tiles, num_tiles;
   float score_log2;  // scale * log2(e), rounded once to fp32
   int32_t out_f32;
   unsigned int* status_word;

@@ -357,7 +357,8 @@ __device__ __forceinline__ void load_w4(const RowParams& p, int j, int n, bool w
   load_w4_kind(p, W == kKindRuntime ? p.w_kind : W, j, n, wvec, w);
 }
 
-// Launches a row kernel, as clusters of rp.cl CTAs when rp.cl > 1.
+// Launches a row kernel, as clusters of rp.cl CTAs when rp.cl > 1 (a launch
+// error is left for the caller's cudaGetLastError).
 template <typename K>
 inline void launch_row_kernel(K kernel, const RowParams& rp, dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream) {
