@@ -467,6 +467,21 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
                    binding.bi_attention_ws(ql[:1], kl[:1], vl[:1], 1.0 / 16), ol[:1])}
     del ql, kl, vl, ol, oc, ws
     out["attention_long"] = long_pt
+    # head dimensions 64, 128, 256 at the workload's token count (B = 32: 256
+    # heads x 816 queries and keys), scale D^-1/2, bf16 out (as SDPA's)
+    dims = []
+    for d in (64, 128, 256):
+        qd, kd, vd = inputs.attention(32, d=d, device="cuda")
+        Ld = qd.shape[0]
+        od = torch.empty(Ld, 816, d, dtype=torch.bfloat16, device="cuda")
+        td = measure(lambda: binding.bi_attention(qd, kd, vd, d ** -0.5, out=od), flush_buf, stream, reps)
+        tsd = measure(lambda: torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, scale=d ** -0.5),
+                      flush_buf, stream, reps)
+        fd = 4.0 * Ld * 816 * 816 * d
+        bd = Ld * 4 * 2.0 * 816 * d
+        dims.append({"D": d, "heads": Ld, "T": 816, "fused": point(fd, bd, td), "sdpa_us": round(tsd * 1e6, 2)})
+        del qd, kd, vd, od
+    out["attention_head_dims"] = dims
     out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0),
                         "fused_head0_bit_equal_all_B": all(bits_equal(of0[B], of0[1]) for B in of0),
                         "sdpa_head0_bit_equal_all_B": all(bits_equal(sd0[B], sd0[1]) for B in sd0)}

@@ -204,11 +204,12 @@ bi_status bi_softmax_lastdim(const bi_tensor* s, const bi_tensor* p, bi_stream s
  * rounded once to o's type.  None of it depends on L, Tq, the tile a row
  * falls in or the SM count: a head alone gives the bits it gives in any
  * batch, and a query row the bits it gives among any other query rows.
- *   q: [L,Tq,256], k and v: [L,Tk,256], bf16, unit stride on the head
+ *   q: [L,Tq,D], k and v: [L,Tk,D], bf16, unit stride on the head
  *   dimension, 16-byte aligned bases, row and batch strides multiples of 16
- *   bytes;  o: [L,Tq,256] fp32 or bf16 (same layout rules);  scale finite.
- *   Tk >= 1 (BI_ERR_INVALID_ARG otherwise); L == 0 or Tq == 0 launches
- *   nothing.  Non-causal, no mask; head dimension 256 only.
+ *   bytes;  o: [L,Tq,D] fp32 or bf16 (same layout rules);  scale finite.
+ *   Head dimension D = 64, 128 or 256 (BI_ERR_INVALID_ARG otherwise); Tk >= 1
+ *   (BI_ERR_INVALID_ARG otherwise); L == 0 or Tq == 0 launches nothing.
+ *   Non-causal, no mask.
  */
 bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
                        const bi_tensor* o, bi_stream stream);
@@ -226,13 +227,14 @@ bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* 
  * workspace; bi_attention refuses a longer key range (BI_ERR_INVALID_ARG).
  *
  * Bytes of workspace bi_attention_ws needs for [L, Tq] queries against Tk
- * keys: 0 when Tk <= 2048, else ceil(Tk / 2048) * L * Tq * 258 * 4.
+ * keys of head dimension D: 0 when Tk <= 2048 (or any argument is out of
+ * range), else ceil(Tk / 2048) * L * Tq * (D + 2) * 4.
  */
-int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk);
+int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk, int64_t D);
 
 /*
  * bi_attention with a caller-owned device workspace (16-byte aligned, at
- * least bi_attention_workspace_bytes(L, Tq, Tk) bytes; may be NULL when that
+ * least bi_attention_workspace_bytes(L, Tq, Tk, D) bytes; may be NULL when that
  * is 0).  The workspace is scratch: its contents on entry do not matter and
  * on return are unspecified; it must not be used by other work on the device
  * while the call's kernels run (stream order).  Results for Tk <= 2048 are

@@ -116,7 +116,7 @@ def load(path: str | None = None):
                 "bi_log_softmax_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_mean_lastdim": ([ptr, ptr, ctypes.c_void_p], st),
                 "bi_attention": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
-                "bi_attention_workspace_bytes": ([ctypes.c_int64] * 3, ctypes.c_int64),
+                "bi_attention_workspace_bytes": ([ctypes.c_int64] * 4, ctypes.c_int64),
                 "bi_attention_noalloc": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p], st),
                 "bi_attention_ws": ([ptr, ptr, ptr, ctypes.c_float, ptr, ctypes.c_void_p, ctypes.c_int64,
                                      ctypes.c_void_p], st),
@@ -293,8 +293,9 @@ def bi_mean_lastdim(x: torch.Tensor, out: torch.Tensor | None = None,
 def bi_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
                  out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
                  stream=None) -> torch.Tensor:
-    """Fused attention softmax(scale * q k^T) v per head: q [L, Tq, 256], k / v
-    [L, Tk, 256] bf16; returns [L, Tq, 256] (fp32 unless out / out_dtype)."""
+    """Fused attention softmax(scale * q k^T) v per head: q [L, Tq, D], k / v
+    [L, Tk, D] bf16, D = 64, 128 or 256; returns [L, Tq, D] (fp32 unless out /
+    out_dtype)."""
     lib = load()
     if out is None:
         out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=out_dtype, device=q.device)
@@ -304,20 +305,20 @@ def bi_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     return out
 
 
-def bi_attention_workspace_bytes(L: int, Tq: int, Tk: int) -> int:
-    return int(load().bi_attention_workspace_bytes(int(L), int(Tq), int(Tk)))
+def bi_attention_workspace_bytes(L: int, Tq: int, Tk: int, D: int = 256) -> int:
+    return int(load().bi_attention_workspace_bytes(int(L), int(Tq), int(Tk), int(D)))
 
 
 def bi_attention_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float,
                     out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Fused attention for any key range: for Tk > 2048 a workspace of
-    bi_attention_workspace_bytes(L, Tq, Tk) bytes is used (allocated here when
+    bi_attention_workspace_bytes(L, Tq, Tk, D) bytes is used (allocated here when
     not given)."""
     lib = load()
     if out is None:
         out = torch.empty((q.shape[0], q.shape[1], q.shape[2]), dtype=out_dtype, device=q.device)
-    need = bi_attention_workspace_bytes(q.shape[0], q.shape[1], k.shape[1])
+    need = bi_attention_workspace_bytes(q.shape[0], q.shape[1], k.shape[1], q.shape[2])
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None else None)

@@ -812,7 +812,7 @@ bi_status attention_impl(const bi_tensor* q, const bi_tensor* k, const bi_tensor
   if (q->dtype != BI_BF16 || k->dtype != BI_BF16 || v->dtype != BI_BF16)
     return finish(BI_ERR_UNSUPPORTED_DTYPE, "q, k and v must be bf16");
   if (o->dtype != BI_F32 && o->dtype != BI_BF16) return finish(BI_ERR_UNSUPPORTED_DTYPE, "o must be fp32 or bf16");
-  if (D != 256) return finish(BI_ERR_INVALID_ARG, "head dimension must be 256");
+  if (!attention_head_dim_ok(D)) return finish(BI_ERR_INVALID_ARG, "head dimension must be 64, 128 or 256");
   if (!std::isfinite(scale)) return finish(BI_ERR_INVALID_ARG, "scale must be finite");
   if (L == 0 || Tq == 0) return finish(BI_OK, why);
   if (Tk == 0) return finish(BI_ERR_INVALID_ARG, "softmax over an empty key range is undefined");
@@ -846,9 +846,9 @@ bi_status attention_impl(const bi_tensor* q, const bi_tensor* k, const bi_tensor
   ap.ws = ws;
   ap.ws_bytes = ws_bytes;
   if (ws && !aligned(ws, 16)) return finish(BI_ERR_UNSUPPORTED_LAYOUT, "the workspace must be 16-byte aligned");
-  if (attention_splits(Tk) > 1 && (!ws || ws_bytes < attention_workspace_bytes(L, Tq, Tk)))
+  if (attention_splits(Tk) > 1 && (!ws || ws_bytes < attention_workspace_bytes(L, Tq, Tk, D)))
     return finish(BI_ERR_INVALID_ARG, "a key range longer than 2048 needs a workspace of " +
-                                          std::to_string(attention_workspace_bytes(L, Tq, Tk)) +
+                                          std::to_string(attention_workspace_bytes(L, Tq, Tk, D)) +
                                           " bytes (bi_attention_workspace_bytes)");
   st = launch_attention(ap, (cudaStream_t)stream, &why);
   return finish(st, why);
@@ -856,9 +856,9 @@ bi_status attention_impl(const bi_tensor* q, const bi_tensor* k, const bi_tensor
 
 }  // namespace
 
-extern "C" int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk) {
-  if (L <= 0 || Tq <= 0 || Tk <= 0) return 0;
-  return attention_workspace_bytes(L, Tq, Tk);
+extern "C" int64_t bi_attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk, int64_t D) {
+  if (L <= 0 || Tq <= 0 || Tk <= 0 || !attention_head_dim_ok(D)) return 0;
+  return attention_workspace_bytes(L, Tq, Tk, D);
 }
 
 extern "C" bi_status bi_attention(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
@@ -893,7 +893,9 @@ extern "C" bi_status bi_attention_noalloc(const bi_tensor* q, const bi_tensor* k
   bi_status st;
   if ((st = check_tensor(q, "q", 3, &why)) != BI_OK) return finish(st, why);
   if ((st = check_tensor(k, "k", 3, &why)) != BI_OK) return finish(st, why);
-  const int64_t need = attention_workspace_bytes(q->shape[0], q->shape[1], k->shape[1]);
+  const int64_t need = attention_head_dim_ok(q->shape[2])
+                           ? attention_workspace_bytes(q->shape[0], q->shape[1], k->shape[1], q->shape[2])
+                           : 0;  // attention_impl reports the head dimension
   if (q->shape[0] == 0 || q->shape[1] == 0 || k->shape[1] == 0 || need == 0)
     return attention_impl(q, k, v, scale, o, nullptr, 0, stream);
   if (need > kNoAllocScratchBytes)
@@ -988,4 +990,4 @@ extern "C" const char* bi_status_string(bi_status s) {
 
 extern "C" const char* bi_last_error_message(void) { return t_last_error.c_str(); }
 
-extern "C" int32_t bi_abi_version(void) { return 7; }
+extern "C" int32_t bi_abi_version(void) { return 8; }

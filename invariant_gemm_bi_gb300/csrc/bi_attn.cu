@@ -50,47 +50,52 @@ namespace bi {
 
 constexpr int kAttnBM = 128;  // query rows per tile
 constexpr int kAttnBN = 128;  // keys per block
-constexpr int kAttnD = 256;   // head dimension
-#ifndef BI_ATTN_STAGE_KB
-#define BI_ATTN_STAGE_KB 32
-#endif
-// A stage holds kAttnKC 16 KB pieces: of a K block, D columns of 64 for all
-// 128 keys; of a V block, 32 keys with all 256 D columns.
-constexpr int kAttnKC = BI_ATTN_STAGE_KB / 16;
-constexpr int kAttnStageBytes = kAttnKC * 16384;
-constexpr int kAttnStages = 131072 / kAttnStageBytes;
-constexpr int kAttnVKeys = 32 * kAttnKC;  // keys of V per stage
 constexpr int kAttnThreads = 320;
 constexpr int kAttnSoftmaxWarps = 8;
-constexpr uint32_t kAttnTmemCols = 512;  // S buffers at columns 0 and 128, O at 256
+constexpr uint32_t kAttnTmemCols = 512;  // S buffers at columns 0 and 128, O from 256
 constexpr uint32_t kAttnOCol = 256;
 constexpr float kAttnRescaleLog2 = 8.0f;  // keep a stale maximum while p <= 2^8
 constexpr int kAttnSplitKeys = 2048;       // key range of one split (a multiple of kAttnBN)
+constexpr int kAttnSmemMax = 232448;       // dynamic shared memory a CTA may use
 
-struct AttnLayout {
-  static constexpr int Q = 0;                                       // 4 x [128 rows x 64 D]
-  static constexpr int OUT = Q + kAttnBM * kAttnD * 2;              // epilogue staging, 4 KB per warp
-  static constexpr int STG = OUT + kAttnSoftmaxWarps * 4096;        // stage ring
-  static constexpr int BARS = STG + kAttnStages * kAttnStageBytes;  // mbarriers
-  static constexpr int NBARS = 11 + 2 * kAttnStages;
-  static constexpr int XCH = BARS + 8 * NBARS;    // running-sum exchange, 2 x 128 floats
-  static constexpr int SLOT = XCH + 2 * kAttnBM * 4;  // TMEM address, abort flag
-  static constexpr int DYN = SLOT + 16 + 1024;   // + alignment slack
+// The shapes that follow the head dimension D (64, 128 or 256).  A ring stage
+// holds kKC 16 KB pieces: of a K block, 64 columns of D for all 128 keys; of
+// a V block, kVKeys keys with all D columns.  The ring takes what shared
+// memory is left beside q and the output staging.
+template <int D>
+struct AttnCfg {
+  static constexpr int kChunks = D / 64;  // 64-column chunks of D (TMA boxes, swizzle atoms)
+  static constexpr int kKC = D >= 128 ? 2 : 1;
+  static constexpr int kStageBytes = kKC * 16384;
+  static constexpr int kKStages = kChunks / kKC;  // ring stages per K block
+  static constexpr int kVKeys = kStageBytes / (D * 2) < kAttnBN ? kStageBytes / (D * 2) : kAttnBN;
+  static constexpr int Q = 0;                        // kChunks x [128 rows x 64 D]
+  static constexpr int OUT = Q + kAttnBM * D * 2;    // epilogue staging, 4 KB per warp
+  static constexpr int STG = OUT + kAttnSoftmaxWarps * 4096;
+  static constexpr int kStages = (kAttnSmemMax - 3072 - STG) / kStageBytes;
+  static constexpr int BARS = STG + kStages * kStageBytes;  // mbarriers
+  static constexpr int NBARS = 11 + 2 * kStages;
+  static constexpr int XCH = BARS + 8 * NBARS;         // running-sum exchange, 2 x 128 floats
+  static constexpr int SLOT = XCH + 2 * kAttnBM * 4;   // TMEM address, abort flag
+  static constexpr int DYN = SLOT + 16 + 1024;         // + alignment slack
+  static_assert(D == 64 || D == 128 || D == 256, "head dimension 64, 128 or 256");
+  static_assert(DYN <= kAttnSmemMax, "attention shared memory exceeds 227 KB");
+  static_assert(kStages >= 4, "at least four ring stages");
 };
-static_assert(AttnLayout::DYN <= 232448, "attention shared memory exceeds 227 KB");
 
 struct AttnBars {
   uint32_t b;
+  int st;  // ring stages
   __device__ __forceinline__ uint32_t q_full() const { return b; }
   __device__ __forceinline__ uint32_t q_empty() const { return b + 8; }
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return b + 16 + 8 * s; }
-  __device__ __forceinline__ uint32_t empty(uint32_t s) const { return b + 16 + 8 * kAttnStages + 8 * s; }
-  __device__ __forceinline__ uint32_t s_full(uint32_t i) const { return b + 16 + 16 * kAttnStages + 8 * i; }
-  __device__ __forceinline__ uint32_t p_full() const { return b + 48 + 16 * kAttnStages; }
-  __device__ __forceinline__ uint32_t pv_done() const { return b + 56 + 16 * kAttnStages; }
-  __device__ __forceinline__ uint32_t o_full() const { return b + 64 + 16 * kAttnStages; }
-  __device__ __forceinline__ uint32_t o_free() const { return b + 72 + 16 * kAttnStages; }
-  __device__ __forceinline__ uint32_t drain() const { return b + 80 + 16 * kAttnStages; }
+  __device__ __forceinline__ uint32_t empty(uint32_t s) const { return b + 16 + 8 * st + 8 * s; }
+  __device__ __forceinline__ uint32_t s_full(uint32_t i) const { return b + 16 + 16 * st + 8 * i; }
+  __device__ __forceinline__ uint32_t p_full() const { return b + 48 + 16 * st; }
+  __device__ __forceinline__ uint32_t pv_done() const { return b + 56 + 16 * st; }
+  __device__ __forceinline__ uint32_t o_full() const { return b + 64 + 16 * st; }
+  __device__ __forceinline__ uint32_t o_free() const { return b + 72 + 16 * st; }
+  __device__ __forceinline__ uint32_t drain() const { return b + 80 + 16 * st; }
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -98,12 +103,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// V stages (kAttnVKeys keys each) of key block j that hold at least one key
+// V stages (kVKeys keys each) of key block j that hold at least one key
 // < Tk; a stage's worth of keys wholly past Tk is neither loaded nor
 // multiplied.
+template <int D>
 __device__ __forceinline__ int attn_v_stages(int j, int Tk) {
+  constexpr int V = AttnCfg<D>::kVKeys;
   const int left = Tk - j * kAttnBN;
-  return left >= kAttnBN ? kAttnBN / kAttnVKeys : (left + kAttnVKeys - 1) / kAttnVKeys;
+  return left >= kAttnBN ? kAttnBN / V : (left + V - 1) / V;
 }
 
 // A work unit: head l, query rows q0 .. q0+127, and keys k0 .. k0+tk-1 (split
@@ -130,38 +137,40 @@ __device__ __forceinline__ AttnTile attn_tile(const AttnParams& p, int tile) {
 // Producer (one thread): per tile the q tile, then K_0, and for each block j
 // K_{j+1} (if any) followed by V_j -- the order the MMA issuer consumes them.
 // ---------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBars& bars, uint32_t sQ,
                                               uint32_t sS, const WaitCtl& wc) {
+  using C = AttnCfg<D>;
   uint32_t it = 0;
   int q_loads = 0;
   bool ok = true;
   auto next_stage = [&](uint32_t& dst, uint32_t& bar) -> bool {
-    const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+    const uint32_t s = it % C::kStages, r = it / C::kStages;
     if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word, wc.limit_ns,
                                     status_code(6, kSiteProducerEmpty)))
       return false;
-    dst = sS + s * kAttnStageBytes;
+    dst = sS + s * C::kStageBytes;
     bar = bars.full(s);
-    mbar_arrive_expect_tx(bar, kAttnStageBytes);
+    mbar_arrive_expect_tx(bar, C::kStageBytes);
     ++it;
     return true;
   };
   auto load_k = [&](int j, const AttnTile& t) -> bool {  // all keys of block j, D columns 64c.. per piece
-    for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
+    for (int cs = 0; cs < C::kKStages; ++cs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
-      for (int b = 0; b < kAttnKC; ++b)
-        tma_load_3d(dst + b * 16384, &p.tma_k, bar, (cs * kAttnKC + b) * 64, t.k0 + j * kAttnBN, t.l);
+      for (int b = 0; b < C::kKC; ++b)
+        tma_load_3d(dst + b * 16384, &p.tma_k, bar, (cs * C::kKC + b) * 64, t.k0 + j * kAttnBN, t.l);
     }
     return true;
   };
-  auto load_v = [&](int j, const AttnTile& t) -> bool {  // kAttnVKeys keys of block j per stage, all D
-    const int nst = attn_v_stages(j, t.tk);
+  auto load_v = [&](int j, const AttnTile& t) -> bool {  // kVKeys keys of block j per stage, all D
+    const int nst = attn_v_stages<D>(j, t.tk);
     for (int vs = 0; vs < nst; ++vs) {
       uint32_t dst, bar;
       if (!next_stage(dst, bar)) return false;
-      for (int c = 0; c < 4; ++c)
-        tma_load_3d(dst + c * (kAttnVKeys * 128), &p.tma_v, bar, c * 64, t.k0 + j * kAttnBN + vs * kAttnVKeys,
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_3d(dst + c * (C::kVKeys * 128), &p.tma_v, bar, c * 64, t.k0 + j * kAttnBN + vs * C::kVKeys,
                     t.l);
     }
     return true;
@@ -175,8 +184,8 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
       ok = false;
       break;
     }
-    mbar_arrive_expect_tx(bars.q_full(), kAttnBM * kAttnD * 2);
-    for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * 16384, &p.tma_q, bars.q_full(), c * 64, q0, l);
+    mbar_arrive_expect_tx(bars.q_full(), kAttnBM * D * 2);
+    for (int c = 0; c < C::kChunks; ++c) tma_load_3d(sQ + c * 16384, &p.tma_q, bars.q_full(), c * 64, q0, l);
     ++q_loads;
     ok = load_k(0, t);
     for (int j = 0; ok && j < t.nkb; ++j) {
@@ -188,9 +197,9 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
   if (q_loads > 0)
     mbar_wait_bounded(bars.q_full(), (q_loads - 1) & 1, nullptr, wc.status_word, wc.limit_ns,
                       status_code(6, kSiteDrain));
-  const uint32_t first = it > (uint32_t)kAttnStages ? it - kAttnStages : 0u;
+  const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
   for (uint32_t j = first; j < it; ++j)
-    if (!mbar_wait_bounded(bars.full(j % kAttnStages), (j / kAttnStages) & 1, nullptr, wc.status_word,
+    if (!mbar_wait_bounded(bars.full(j % C::kStages), (j / C::kStages) & 1, nullptr, wc.status_word,
                            wc.limit_ns, status_code(6, kSiteDrain)))
       break;
 }
@@ -199,10 +208,12 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, const AttnBar
 // MMA issuer (one thread): S_0; then per block j: S_{j+1} (other S buffer),
 // PV_j once the softmax warps have written P_j.
 // ---------------------------------------------------------------------------
+template <int D>
 __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& bars, uint32_t sQ, uint32_t sS,
                                          uint32_t tmem, const WaitCtl& wc) {
+  using C = AttnCfg<D>;
   const uint32_t kIdS = idesc_bf16_f32(kAttnBM, kAttnBN, false);
-  const uint32_t kIdO = idesc_bf16_f32(kAttnBM, kAttnD, true);
+  const uint32_t kIdO = idesc_bf16_f32(kAttnBM, D, true);
   uint32_t it = 0, sc = 0, pc = 0;
   int local = 0;
   bool ok = true;
@@ -216,14 +227,14 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
   auto issue_s = [&](int j) -> bool {
     const uint32_t buf = sc & 1;
     const uint32_t d = tmem + buf * kAttnBN;
-    for (int cs = 0; cs < 4 / kAttnKC; ++cs) {
-      const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+    for (int cs = 0; cs < C::kKStages; ++cs) {
+      const uint32_t s = it % C::kStages, r = it / C::kStages;
       if (!wait(bars.full(s), r & 1)) return false;
       tc_fence_after_sync();
-      const uint32_t kb = sS + s * kAttnStageBytes;
+      const uint32_t kb = sS + s * C::kStageBytes;
 #pragma unroll
-      for (int b = 0; b < kAttnKC; ++b) {
-        const int c = cs * kAttnKC + b;  // D columns 64c..
+      for (int b = 0; b < C::kKC; ++b) {
+        const int c = cs * C::kKC + b;  // D columns 64c..
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // K = 16 steps over D, ascending
           const uint64_t ad = smem_desc_sw128(sQ + c * 16384 + kk * 32, 16, 1024);
@@ -241,17 +252,17 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
   };
   auto issue_pv = [&](int j) -> bool {
     const uint32_t pbuf = tmem + (pc & 1) * kAttnBN;  // P_j: in the TMEM buffer of S_j
-    const int nst = attn_v_stages(j, tk);
-    for (int vs = 0; vs < nst; ++vs) {  // keys vs * kAttnVKeys.. of the block
-      const uint32_t s = it % kAttnStages, r = it / kAttnStages;
+    const int nst = attn_v_stages<D>(j, tk);
+    for (int vs = 0; vs < nst; ++vs) {  // keys vs * kVKeys.. of the block
+      const uint32_t s = it % C::kStages, r = it / C::kStages;
       if (!wait(bars.full(s), r & 1)) return false;
       tc_fence_after_sync();
-      const uint32_t vb = sS + s * kAttnStageBytes;
+      const uint32_t vb = sS + s * C::kStageBytes;
 #pragma unroll
-      for (int k = 0; k < kAttnVKeys / 16; ++k) {  // K = 16 steps over keys, ascending
-        const int key = vs * kAttnVKeys + 16 * k;  // first key of the step within the block
+      for (int k = 0; k < C::kVKeys / 16; ++k) {  // K = 16 steps over keys, ascending
+        const int key = vs * C::kVKeys + 16 * k;  // first key of the step within the block
         const uint32_t acol = pbuf + (key >> 6) * 64 + ((key & 63) >> 4) * 8;
-        const uint64_t bd = smem_desc_sw128(vb + k * 2048, kAttnVKeys * 128, 1024);
+        const uint64_t bd = smem_desc_sw128(vb + k * 2048, C::kVKeys * 128, 1024);
         umma_bf16_ts(tmem + kAttnOCol, acol, bd, kIdO, (j | vs | k) != 0 ? 1u : 0u);
       }
       umma_commit(bars.empty(s));
@@ -288,10 +299,63 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, const AttnBars& ba
 // Softmax and epilogue (warps 2-9): one query row and one half of the keys /
 // of O's columns per thread.
 // ---------------------------------------------------------------------------
+// A warp's share of the output: its 32 query rows (one per lane, TMEM lanes
+// trow..) x the D / 2 columns of half hc, scaled by rinv and rounded once to
+// the output type, stored to rows 0 .. rows-1 of `out` (row stride ld
+// elements).  The rows are turned around through the warp's 4 KB staging
+// region one piece of PB bytes per row at a time (16-byte unit u of row r at
+// unit u ^ swz(r), conflict-free both ways), so that each store instruction
+// writes whole row segments of PB bytes.
+template <int D, bool F32, typename T>
+__device__ __forceinline__ void attn_store_rows(T* out, int64_t ld, int64_t rows, uint32_t trow, int hc, int lane,
+                                                uint32_t region, float rinv) {
+  constexpr int kHalf = D / 2;
+  constexpr int esz = F32 ? 4 : 2;
+  constexpr int PB = kHalf * esz < 128 ? kHalf * esz : 128;  // bytes of a row per piece
+  constexpr int U = PB / 16;                                 // 16-byte units per piece row
+  constexpr int cols = PB / esz;                             // columns per piece
+  auto swz = [](int r) { return U == 8 ? (r & 7) : ((r >> 1) & 3); };
+#pragma unroll 1
+  for (int c = 0; c < kHalf / cols; ++c) {
+    uint32_t w[PB / 4];
+#pragma unroll
+    for (int h = 0; h < cols / 32; ++h) {
+      uint32_t r[32];
+      tmem_load_32cols(trow + kAttnOCol + hc * kHalf + c * cols + h * 32, r);
+      tmem_load_wait(r);
+      if constexpr (F32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), rinv));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[h * 16 + i] =
+              pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * i]), rinv), __fmul_rn(__uint_as_float(r[2 * i + 1]), rinv));
+      }
+    }
+    __syncwarp();  // the previous piece has been read back
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      st_shared_v4(region + lane * PB + ((u ^ swz(lane)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    __syncwarp();
+    // read back: lane L takes unit L % U of rows (32 / U) i + L / U
+    const int u = lane % U;
+    const int col = hc * kHalf + c * cols + u * (16 / esz);
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int rr = (32 / U) * i + lane / U;
+      const uint4 v = ld_shared_v4(region + rr * PB + ((u ^ swz(rr)) << 4));
+      if (rr < rows) *reinterpret_cast<uint4*>(out + rr * ld + col) = v;
+    }
+  }
+}
+
+template <int D>
 __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars& bars, uint32_t sOut,
                                              float* xch, uint32_t tmem, int warp, int lane, const WaitCtl& wc) {
+  constexpr int kHalf = D / 2;     // O columns per warp
   const int qd = warp & 3;         // TMEM lane quadrant this warp may access
-  const int hc = (warp - 2) >> 2;  // half: keys 64hc.. of a block, O columns 128hc..
+  const int hc = (warp - 2) >> 2;  // half: keys 64hc.. of a block, O columns kHalf hc..
   const int row = qd * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
   const uint32_t pair_bar = 1 + qd;  // named barrier of the quadrant's two warps
@@ -390,8 +454,8 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         tc_fence_after_sync();
         const float f = resc ? alpha : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t oc = trow + kAttnOCol + hc * 128 + c * 32;
+        for (int c = 0; c < kHalf / 32; ++c) {
+          const uint32_t oc = trow + kAttnOCol + hc * kHalf + c * 32;
           uint32_t r[32];
           tmem_load_32cols(oc, r);
           tmem_load_wait(r);
@@ -446,51 +510,16 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
     }
     if (q0 + qd * 32 < p.Tq) {  // warp-uniform: some of its rows are outputs
       const uint32_t region = sOut + (hc * 4 + qd) * 4096;
-      const bool f32 = split || p.out_f32;
-      const int esz = f32 ? 4 : 2;
-      const int cols = 128 / esz;  // columns per 128-byte piece of a row
-      const int64_t ot = split ? kAttnD : p.o_t;
-      char* obase =
-          split ? reinterpret_cast<char*>(p.ws_o + (((int64_t)tl.sp * p.L + l) * p.Tq + q0 + qd * 32) * kAttnD)
-                : static_cast<char*>(p.o) + ((int64_t)l * p.o_l + (int64_t)(q0 + qd * 32) * p.o_t) * esz;
-      for (int c = 0; c < 128 / cols; ++c) {
-        uint32_t w[32];
-        if (f32) {
-          uint32_t r[32];
-          tmem_load_32cols(trow + kAttnOCol + hc * 128 + c * 32, r);
-          tmem_load_wait(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), rinv));
-        } else {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t r[32];
-            tmem_load_32cols(trow + kAttnOCol + hc * 128 + c * 64 + hh * 32, r);
-            tmem_load_wait(r);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[hh * 16 + i] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * i]), rinv),
-                                           __fmul_rn(__uint_as_float(r[2 * i + 1]), rinv));
-          }
-        }
-        __syncwarp();  // the previous piece has been read back
-        // row `lane`, 16-byte unit u at unit u ^ (lane & 7): conflict-free both ways
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(region + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                       w[4 * u + 3]);
-        __syncwarp();
-        // read back: lane L takes unit L % 8 of rows 4i + L / 8
-        const int u = lane & 7;
-        const int col = hc * 128 + c * cols + u * (16 / esz);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + (lane >> 3);
-          const uint4 v = ld_shared_v4(region + rr * 128 + ((u ^ (rr & 7)) << 4));
-          if (q0 + qd * 32 + rr < p.Tq)
-            *reinterpret_cast<uint4*>(obase + ((int64_t)rr * ot + col) * esz) = v;
-        }
-      }
+      const int64_t qrow = q0 + qd * 32;
+      if (split)
+        attn_store_rows<D, true>(p.ws_o + (((int64_t)tl.sp * p.L + l) * p.Tq + qrow) * D, D, p.Tq - qrow, trow,
+                                 hc, lane, region, rinv);
+      else if (p.out_f32)
+        attn_store_rows<D, true>(static_cast<float*>(p.o) + (int64_t)l * p.o_l + qrow * p.o_t, p.o_t,
+                                 p.Tq - qrow, trow, hc, lane, region, rinv);
+      else
+        attn_store_rows<D, false>(static_cast<__nv_bfloat16*>(p.o) + (int64_t)l * p.o_l + qrow * p.o_t, p.o_t,
+                                  p.Tq - qrow, trow, hc, lane, region, rinv);
     }
     tc_fence_before_sync();
     __syncwarp();
@@ -498,16 +527,18 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + AttnLayout::Q;
-  const uint32_t sOut = base + AttnLayout::OUT;
-  const uint32_t sS = base + AttnLayout::STG;
-  const AttnBars bars{base + AttnLayout::BARS};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnLayout::SLOT);
+  const uint32_t sQ = base + C::Q;
+  const uint32_t sOut = base + C::OUT;
+  const uint32_t sS = base + C::STG;
+  const AttnBars bars{base + C::BARS, C::kStages};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -515,7 +546,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full(), 1);
     mbar_init(bars.q_empty(), 1);
-    for (int s = 0; s < kAttnStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
@@ -542,11 +573,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const WaitCtl wc{abort_flag, p.status_word, p.wait_limit_ns};
 
   if (warp == 0) {
-    if (lane == 0) attn_producer(p, bars, sQ, sS, wc);
+    if (lane == 0) attn_producer<D>(p, bars, sQ, sS, wc);
   } else if (warp == 1) {
-    if (lane == 0) attn_mma(p, bars, sQ, sS, tmem, wc);
+    if (lane == 0) attn_mma<D>(p, bars, sQ, sS, tmem, wc);
   } else {
-    attn_softmax(p, bars, sOut, reinterpret_cast<float*>(smem + AttnLayout::XCH), tmem, warp, lane, wc);
+    attn_softmax<D>(p, bars, sOut, reinterpret_cast<float*>(smem + C::XCH), tmem, warp, lane, wc);
   }
 
   tc_fence_before_sync();
@@ -559,12 +590,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// Merge of a split key range, one 256-thread block per (head, query row),
+// Merge of a split key range, one D-thread block per (head, query row),
 // thread d for output column d: M = max over splits of m_s (log2 units);
 // w_s = 2^(m_s - M); l = sum_s RN(w_s l_s), O_d = sum_s RN(w_s O_s,d), both in
 // ascending split order; o_d = RN(O_d * RN(1 / l)), rounded once to o's type.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kAttnD) attn_merge_kernel(const AttnParams p) {
+template <int D>
+__global__ void __launch_bounds__(D) attn_merge_kernel(const AttnParams p) {
   const int64_t rowi = blockIdx.x;  // l * Tq + q
   const int l = (int)(rowi / p.Tq);
   const int q = (int)(rowi - (int64_t)l * p.Tq);
@@ -576,7 +608,7 @@ __global__ void __launch_bounds__(kAttnD) attn_merge_kernel(const AttnParams p) 
   for (int s = 0; s < p.ns; ++s) {
     const float w = ex2_approx(__fsub_rn(p.ws_ml[(s * per_split + rowi) * 2], M));
     const float ls = __fmul_rn(w, p.ws_ml[(s * per_split + rowi) * 2 + 1]);
-    const float os = __fmul_rn(w, p.ws_o[(s * per_split + rowi) * kAttnD + d]);
+    const float os = __fmul_rn(w, p.ws_o[(s * per_split + rowi) * D + d]);
     lsum = s == 0 ? ls : __fadd_rn(lsum, ls);
     o = s == 0 ? os : __fadd_rn(o, os);
   }
@@ -590,31 +622,51 @@ __global__ void __launch_bounds__(kAttnD) attn_merge_kernel(const AttnParams p) 
 
 int64_t attention_splits(int64_t Tk) { return Tk <= kAttnSplitKeys ? 1 : (Tk + kAttnSplitKeys - 1) / kAttnSplitKeys; }
 
-int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk) {
+int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk, int64_t D) {
   const int64_t ns = attention_splits(Tk);
-  return ns == 1 ? 0 : ns * L * Tq * (kAttnD + 2) * (int64_t)sizeof(float);
+  return ns == 1 ? 0 : ns * L * Tq * (D + 2) * (int64_t)sizeof(float);
+}
+
+bool attention_head_dim_ok(int64_t D) { return D == 64 || D == 128 || D == 256; }
+
+template <int D>
+static cudaError_t attn_launch_d(const AttnParams& p, int64_t tiles, int num_sms, cudaStream_t stream) {
+  using C = AttnCfg<D>;
+  const int slot = D == 256 ? 7 : D == 128 ? 12 : 13;  // the GEMMs hold 0-3 and 8-11
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attn_kernel<D>), C::DYN, slot);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<int64_t>(tiles, num_sms);
+  attn_kernel<D><<<grid, kAttnThreads, C::DYN, stream>>>(p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && p.ns > 1) {
+    attn_merge_kernel<D><<<(unsigned)((int64_t)p.L * p.Tq), D, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why) {
   DeviceInfo dev;
   bi_status st = current_device_info(&dev, why);
   if (st != BI_OK) return st;
-  if (ap.D != kAttnD) {
-    *why = "head dimension must be 256";
+  if (!attention_head_dim_ok(ap.D)) {
+    *why = "head dimension must be 64, 128 or 256";
     return BI_ERR_INVALID_ARG;
   }
+  const int D = (int)ap.D;
   AttnParams p;
   memset(&p, 0, sizeof(p));
   auto map_in = [&](CUtensorMap* map, const void* ptr, int64_t T, int64_t st_t, int64_t st_l,
                     uint32_t box_rows) {
-    const cuuint64_t dims[3] = {(cuuint64_t)kAttnD, (cuuint64_t)T, (cuuint64_t)ap.L};
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)ap.L};
     const cuuint64_t strides[2] = {(cuuint64_t)st_t * 2, (cuuint64_t)st_l * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
     return encode_tiled_bf16(map, const_cast<void*>(ptr), 3, dims, strides, box, why);
   };
   if (!map_in(&p.tma_q, ap.q, ap.Tq, ap.q_t, ap.q_l, kAttnBM) ||
       !map_in(&p.tma_k, ap.k, ap.Tk, ap.k_t, ap.k_l, kAttnBN) ||
-      !map_in(&p.tma_v, ap.v, ap.Tk, ap.v_t, ap.v_l, kAttnVKeys))
+      !map_in(&p.tma_v, ap.v, ap.Tk, ap.v_t, ap.v_l,
+              D == 256 ? AttnCfg<256>::kVKeys : D == 128 ? AttnCfg<128>::kVKeys : AttnCfg<64>::kVKeys))
     return BI_ERR_CUDA;
   p.o = ap.o;
   p.o_t = ap.o_t;
@@ -625,14 +677,14 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   p.q_tiles = (int32_t)((ap.Tq + kAttnBM - 1) / kAttnBM);
   p.ns = (int32_t)attention_splits(ap.Tk);
   if (p.ns > 1) {
-    const int64_t need = attention_workspace_bytes(ap.L, ap.Tq, ap.Tk);
+    const int64_t need = attention_workspace_bytes(ap.L, ap.Tq, ap.Tk, D);
     if (!ap.ws || ap.ws_bytes < need) {
       *why = "a key range longer than " + std::to_string(kAttnSplitKeys) + " needs a workspace of " +
              std::to_string(need) + " bytes";
       return BI_ERR_INVALID_ARG;
     }
     p.ws_o = static_cast<float*>(ap.ws);
-    p.ws_ml = p.ws_o + p.ns * ap.L * ap.Tq * kAttnD;
+    p.ws_ml = p.ws_o + p.ns * ap.L * ap.Tq * D;
   }
   const int64_t tiles = ap.L * (int64_t)p.q_tiles * p.ns;
   if (tiles > INT32_MAX) {
@@ -644,20 +696,13 @@ bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::stri
   p.out_f32 = ap.out_f32;
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attn_kernel), AttnLayout::DYN, 7);
-  if (e == cudaSuccess) {
-    const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
-    attn_kernel<<<grid, kAttnThreads, AttnLayout::DYN, stream>>>(p);
-    e = cudaGetLastError();
+  if (p.ns > 1 && ap.L * ap.Tq > INT32_MAX) {
+    *why = "too many query rows for the split merge";
+    return BI_ERR_INVALID_ARG;
   }
-  if (e == cudaSuccess && p.ns > 1) {
-    if (ap.L * ap.Tq > INT32_MAX) {
-      *why = "too many query rows for the split merge";
-      return BI_ERR_INVALID_ARG;
-    }
-    attn_merge_kernel<<<(unsigned)(ap.L * ap.Tq), kAttnD, 0, stream>>>(p);
-    e = cudaGetLastError();
-  }
+  const cudaError_t e = D == 256   ? attn_launch_d<256>(p, tiles, dev.num_sms, stream)
+                        : D == 128 ? attn_launch_d<128>(p, tiles, dev.num_sms, stream)
+                                   : attn_launch_d<64>(p, tiles, dev.num_sms, stream);
   if (e != cudaSuccess) {
     *why = std::string("attention launch: ") + cudaGetErrorString(e);
     return BI_ERR_CUDA;

@@ -162,7 +162,9 @@ struct AttnProblem {
 bi_status launch_attention(const AttnProblem& ap, cudaStream_t stream, std::string* why);
 // Key-range splits (2048 keys each) and the workspace they need (0 if one).
 int64_t attention_splits(int64_t Tk);
-int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk);
+int64_t attention_workspace_bytes(int64_t L, int64_t Tq, int64_t Tk, int64_t D);
+// The head dimensions the fused attention kernel is built for: 64, 128, 256.
+bool attention_head_dim_ok(int64_t D);
 
 // op: kRowRmsNorm, kRowLogSoftmax or kRowMean.
 bi_status launch_row_reduction(int op, const RowParams& rp, cudaStream_t stream, std::string* why);

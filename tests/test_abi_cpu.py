@@ -49,7 +49,7 @@ def test_library_has_no_oracle_or_host_math_dependency():
 def test_status_strings(lib):
     assert binding.status_string(0) == "BI_OK"
     assert binding.status_string(6) == "BI_ERR_TIMEOUT"
-    assert lib.bi_abi_version() == 7
+    assert lib.bi_abi_version() == 8
 
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
@@ -276,9 +276,11 @@ def test_attention_validation(lib):
     assert call(q, _t([2, 91, 256]), v, o) == binding.BI_ERR_SHAPE_MISMATCH
     assert call(q, k, v, _t([2, 99, 256], dtype=2)) == binding.BI_ERR_SHAPE_MISMATCH
     assert call(q, _t([3, 90, 256]), _t([3, 90, 256]), o) == binding.BI_ERR_SHAPE_MISMATCH
-    # head dimension 256 only; dtypes
-    assert call(_t([2, 100, 128]), _t([2, 90, 128]), _t([2, 90, 128]), _t([2, 100, 128], dtype=2)) == \
-        binding.BI_ERR_INVALID_ARG
+    # head dimension 64, 128 or 256 only; dtypes
+    for d in (32, 96, 192, 512):
+        assert call(_t([2, 100, d]), _t([2, 90, d]), _t([2, 90, d]), _t([2, 100, d], dtype=2)) == \
+            binding.BI_ERR_INVALID_ARG
+        assert "head dimension" in binding.last_error_message()
     assert call(_t([2, 100, 256], dtype=1), k, v, o) == binding.BI_ERR_UNSUPPORTED_DTYPE
     assert call(q, k, v, _t([2, 100, 256], dtype=1)) == binding.BI_ERR_UNSUPPORTED_DTYPE
     # layouts: non-unit head stride, a row stride that is not 16 bytes, a misaligned base
@@ -299,14 +301,16 @@ def test_attention_validation(lib):
 
 
 def test_attention_workspace_rules(lib):
-    # no workspace up to 2048 keys; ceil(Tk / 2048) splits of L*Tq*(256+2) floats beyond
-    assert lib.bi_attention_workspace_bytes(2, 100, 2048) == 0
-    assert lib.bi_attention_workspace_bytes(2, 100, 2049) == 2 * 2 * 100 * 258 * 4
-    assert lib.bi_attention_workspace_bytes(3, 7, 6145) == 4 * 3 * 7 * 258 * 4
-    assert lib.bi_attention_workspace_bytes(0, 7, 6145) == 0
+    # no workspace up to 2048 keys; ceil(Tk / 2048) splits of L*Tq*(D+2) floats beyond
+    for d in (64, 128, 256):
+        assert lib.bi_attention_workspace_bytes(2, 100, 2048, d) == 0
+        assert lib.bi_attention_workspace_bytes(2, 100, 2049, d) == 2 * 2 * 100 * (d + 2) * 4
+        assert lib.bi_attention_workspace_bytes(3, 7, 6145, d) == 4 * 3 * 7 * (d + 2) * 4
+        assert lib.bi_attention_workspace_bytes(0, 7, 6145, d) == 0
+    assert lib.bi_attention_workspace_bytes(2, 100, 6145, 96) == 0  # no such kernel
     q, k, v, o = _t([2, 100, 256]), _t([2, 3000, 256]), _t([2, 3000, 256]), _t([2, 100, 256], dtype=2)
     f = ctypes.c_float(0.0625)
-    need = lib.bi_attention_workspace_bytes(2, 100, 3000)
+    need = lib.bi_attention_workspace_bytes(2, 100, 3000, 256)
     # a long key range without (enough) workspace is refused before any launch
     assert lib.bi_attention(_r(q), _r(k), _r(v), f, _r(o), None) == binding.BI_ERR_INVALID_ARG
     assert "workspace" in binding.last_error_message()

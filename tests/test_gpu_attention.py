@@ -41,10 +41,10 @@ def _lib():
     assert binding.bi_device_status() == binding.BI_OK
 
 
-def _qkv(L, Tq, Tk, seed):
-    q = inputs.normal_bf16((L, Tq, D), 1.0, seed)
-    k = inputs.normal_bf16((L, Tk, D), 1.0, seed + 1)
-    v = inputs.normal_bf16((L, Tk, D), 1.0, seed + 2)
+def _qkv(L, Tq, Tk, seed, d=D):
+    q = inputs.normal_bf16((L, Tq, d), 1.0, seed)
+    k = inputs.normal_bf16((L, Tk, d), 1.0, seed + 1)
+    v = inputs.normal_bf16((L, Tk, d), 1.0, seed + 2)
     return q, k, v
 
 
@@ -220,3 +220,82 @@ def test_attention_unsplit_range_is_the_same_with_or_without_workspace():
     with pytest.raises(binding.BiError) as ei:
         binding.bi_attention(qg, torch.cat([kg, kg[:, :1]], 1), torch.cat([vg, vg[:, :1]], 1), 0.0625)
     assert ei.value.status == binding.BI_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# Head dimensions 64 and 128: the same kernel built for a narrower D (fewer
+# tensor-core steps per score, a narrower O), held to the same bar
+# ---------------------------------------------------------------------------
+
+SMALL_D = [64, 128]
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 129, 64), (3, 200, 333), (2, 816, 816)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_attention_head_dims_match_oracle(d, shape, out_dtype):
+    L, Tq, Tk = shape
+    q, k, v = _qkv(L, Tq, Tk, 70, d)
+    scale = d ** -0.5
+    ref, absum, smax = oracle.attention(q, k, v, scale)
+    o = binding.bi_attention(q.cuda(), k.cuda(), v.cuda(), scale, out_dtype=out_dtype)
+    check_attention(o, ref, absum, smax, Tk, f"attention D={d} {shape} -> {out_dtype}")
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+def test_attention_head_dims_rescale(d):
+    L, Tq, Tk = 2, 130, 700
+    q = (torch.ones(L, Tq, d) * 0.5).to(torch.bfloat16)
+    ramp = torch.arange(Tk, dtype=torch.float32) / 10.0
+    k = (ramp[None, :, None] * torch.ones(L, Tk, d)).to(torch.bfloat16)
+    k[:, :, 1::2] *= -0.5
+    v = inputs.normal_bf16((L, Tk, d), 1.0, 71)
+    ref, absum, smax = oracle.attention(q, k, v, 0.2)
+    o = binding.bi_attention(q.cuda(), k.cuda(), v.cuda(), 0.2)
+    check_attention(o, ref, absum, smax, Tk, f"rescale D={d}")
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+def test_attention_head_dims_invariances(d):
+    # heads alone vs in a batch of 40 (more tiles than SMs), query chunks, run to run
+    q, k, v = _qkv(40, 300, 450, 72, d)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    full = binding.bi_attention(qg, kg, vg, d ** -0.5)
+    for h in (0, 17, 39):
+        assert bits_equal(binding.bi_attention(qg[h:h + 1], kg[h:h + 1], vg[h:h + 1], d ** -0.5), full[h:h + 1]), h
+    for a, b in ((0, 1), (127, 129), (200, 300)):
+        assert bits_equal(binding.bi_attention(qg[:, a:b].contiguous(), kg, vg, d ** -0.5), full[:, a:b]), (a, b)
+    assert bits_equal(binding.bi_attention(qg, kg, vg, d ** -0.5), full)
+    ref, absum, smax = oracle.attention(q[38:40], k[38:40], v[38:40], d ** -0.5)
+    check_attention(full[38:40], ref, absum, smax, 450, f"D={d} heads 38-39")
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_attention_head_dims_strided(d, out_dtype):
+    # packed [L, T, 3, d] operands and a padded output: the bits of contiguous ones
+    L, T = 3, 250
+    g = inputs.normal_bf16((L, T, 3, d), 1.0, 73).cuda()
+    q, k, v = g[:, :, 0], g[:, :, 1], g[:, :, 2]
+    ref_o = binding.bi_attention(q.contiguous(), k.contiguous(), v.contiguous(), 0.125, out_dtype=out_dtype)
+    big = torch.full((L, T + 3, d + 64), 7.0, device="cuda", dtype=out_dtype)
+    out = big[:, 1:T + 1, 32:32 + d]
+    binding.bi_attention(q, k, v, 0.125, out=out)
+    assert bits_equal(out.contiguous(), ref_o)
+    assert bool((big[:, 0] == 7.0).all()) and bool((big[:, T + 1:] == 7.0).all())
+    assert bool((big[:, :, :32] == 7.0).all()) and bool((big[:, :, 32 + d:] == 7.0).all())
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_attention_head_dims_split(d, out_dtype):
+    L, Tq, Tk = 3, 140, 4500
+    q, k, v = _qkv(L, Tq, Tk, 74, d)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    assert binding.bi_attention_workspace_bytes(L, Tq, Tk, d) == 3 * L * Tq * (d + 2) * 4
+    full = binding.bi_attention_ws(qg, kg, vg, d ** -0.5, out_dtype=out_dtype)
+    ref, absum, smax = oracle.attention(q, k, v, d ** -0.5)
+    check_attention(full, ref, absum, smax, Tk, f"split D={d} -> {out_dtype}")
+    assert bits_equal(binding.bi_attention_ws(qg[1:2], kg[1:2], vg[1:2], d ** -0.5, out_dtype=out_dtype), full[1:2])
+    assert bits_equal(binding.bi_attention_ws(qg[:, 130:].contiguous(), kg, vg, d ** -0.5, out_dtype=out_dtype),
+                      full[:, 130:])

@@ -31,7 +31,7 @@ def _t(shape, dtype=0, ptr=0x7F0000000000):
 def test_noalloc_refuses_a_workspace_larger_than_the_scratch():
     lib = binding.load()
     L, Tq, Tk = 8, 8192, 8192
-    assert lib.bi_attention_workspace_bytes(L, Tq, Tk) > SCRATCH
+    assert lib.bi_attention_workspace_bytes(L, Tq, Tk, 256) > SCRATCH
     q, k, v, o = _t([L, Tq, D]), _t([L, Tk, D]), _t([L, Tk, D]), _t([L, Tq, D], dtype=2)
     st = lib.bi_attention_noalloc(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_float(0.0625),
                                   ctypes.byref(o), None)
