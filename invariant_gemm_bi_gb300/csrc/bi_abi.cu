@@ -655,8 +655,8 @@ extern "C" bi_status bi_conv2d_patch_packed(const bi_tensor* x, const bi_conv_pa
   // The image is read as whole rows by TMA: 16-byte rows, at most 256 wide,
   // and one K block's rows (4 kernel rows of each output row of a tile) must
   // fit one staging buffer.
-  const int64_t t_oh = std::min<int64_t>(Ho, 128 / std::max<int64_t>(Wo, 1));
-  if ((W * 2) % 16 != 0 || W > 256 || Wo > 128 || W * 4 * t_oh * 2 > kPatchStageMax)
+  const int64_t t_oh = patch_tile_rows(Ho, Wo, W);
+  if ((W * 2) % 16 != 0 || W > 256 || Wo > 128 || patch_stage_bytes(W, t_oh) > kPatchStageMax)
     return fail(BI_ERR_UNSUPPORTED_LAYOUT,
                 "image rows must be a multiple of 8 and at most 256 elements, with W/KW <= 128");
   if (!x->ptr || !y->ptr) return fail(BI_ERR_INVALID_ARG, "null data pointer");

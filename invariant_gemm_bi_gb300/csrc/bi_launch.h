@@ -140,6 +140,12 @@ struct PatchProblem {
 };
 // Row length of the packed filter: C * (KH rounded up to 4) * 16.
 int64_t patch_padded_k(int64_t C, int64_t KH);
+// Shared memory of one staged K block of image rows (t_oh output rows of an
+// image W pixels wide); at most kPatchStageMax.
+int64_t patch_stage_bytes(int64_t W, int64_t t_oh);
+// Output rows per tile: whole rows, at most 128 positions, one staged block
+// within kPatchStageMax.  A function of the image shape only.
+int64_t patch_tile_rows(int64_t Ho, int64_t Wo, int64_t W);
 bi_status launch_conv_pack(const void* w, void* dst, int64_t Co, int64_t C, int64_t KH, int64_t KW,
                            cudaStream_t stream, std::string* why);
 bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string* why);

@@ -13,96 +13,148 @@
 // are zero on both sides.  One tensor-core K = 16 step is thus one kernel row,
 // and a 64-wide K block is four rows (ci, kh0 .. kh0+3) of one channel.
 //
-// No unfolded matrix exists anywhere.  Per K block the producer TMA-loads,
+// No unfolded matrix exists anywhere.  Per K block the producers TMA-load,
 // for the tile's t_oh output rows, the four image rows (ci, oh*KH + kh0 ..
 // +3) of the sample -- whole rows, 16-byte aligned, rows past KH zero-filled
-// by the copy engine -- and the [256 x 64] block of the packed filter.  Four
-// warps then rebuild the K-major, 128-byte-swizzled patch tile (one tile row
-// per output position) from the staged rows in shared memory, writing zeros
-// for kw >= KW; the UMMA issue loop and the epilogue are the GEMM's.  A tile
-// is (sample, block of t_oh output rows, 256 channels): it never mixes
-// samples, so one sample's arithmetic is the same for every batch size.
+// by the copy engine -- and the [192 x 64] block of the packed filter.  Four
+// builder warps then turn the staged rows into the patch tile (one row per
+// output position, zeros for kw >= KW) and write it straight into tensor
+// memory, where the MMA takes its A operand: the tile never passes through
+// shared memory, whose bandwidth (image rows in and out, filter in and out)
+// is what bounds this kernel.  A tile is (sample, block of t_oh output rows,
+// 192 channels): it never mixes samples, so one sample's arithmetic is the
+// same for every batch size.
 //
-//   warp 0      producer: image rows (staging ring) and filter blocks (TMA)
-//   warp 1      TMEM allocator + UMMA issuer (128 x 256 x 16, cta_group::1)
+//   warp 0      filter producer (TMA, a ring of 4 stages)
+//   warp 1      TMEM allocator + UMMA issuer (128 x 192 x 16, cta_group::1,
+//               A from TMEM, B = the filter block from shared memory)
 //   warps 2..5  epilogue: tcgen05.ld -> + bias -> rounding -> y (NCHW: the
 //               32 threads of a warp write 32 consecutive positions of a
 //               channel per store)
-//   warps 6..9  patch-tile builders
+//   warps 6..9  patch-tile builders (warp w writes TMEM lanes 32 (w % 4) ..)
+//   warp 10     image-row producer (TMA, a ring of up to 8 staged blocks: a
+//               copy from L2 takes about a microsecond, several K blocks'
+//               worth, so the rows are fetched well ahead of the filter)
+//
+// TMEM: accumulators at columns 0 and 192 (the epilogue of one tile overlaps
+// the next tile's MMAs), patch-tile stages of 32 columns (64 bf16 k per
+// position) from column 384.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "bi_common.h"
 #include "bi_launch.h"
 #include "bi_ptx.cuh"
+#include "bi_ptx_ext.cuh"
 #include "bi_roles.cuh"
 
 namespace bi {
 
+constexpr int kPatchBN = 192;  // output channels per tile
+
 struct PatchLayout {
-  static constexpr int A_BYTES = kBM * kBK * 2;  // 128 positions x 64 k
-  static constexpr int B_BYTES = kBN * kBK * 2;  // 256 channels x 64 k
-  static constexpr int STAGES = 3;
-  static constexpr int STG_BUFS = 2;
+  static constexpr int B_BYTES = kPatchBN * kBK * 2;  // 192 channels x 64 k
+  static constexpr int STAGES = 4;                    // K blocks in flight (filter + TMEM patch tile)
+  static constexpr int STG_BUFS = 8;                  // staged image-row blocks, at most
+  static constexpr int STG_REGION = 128 * 1024;       // holds min(8, region / block) blocks (>= 4)
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int DYN_BYTES =
-      1024 + STAGES * (A_BYTES + B_BYTES) + STG_BUFS * kPatchStageMax + BAR_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2 * kBN;
+  static constexpr int DYN_BYTES = 1024 + STAGES * B_BYTES + STG_REGION + BAR_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t A_COL = 2 * kPatchBN;     // first patch-tile stage column
+  static_assert(A_COL + STAGES * (kBK / 2) <= TMEM_COLS, "accumulators and patch stages fit TMEM");
   static_assert(DYN_BYTES <= 232448, "fits the opt-in shared memory of one CTA");
   static_assert(DYN_BYTES > 116 * 1024, "one CTA per SM: TMEM is allocated whole");
   static_assert(8 * (2 * STAGES + 2 * STG_BUFS + 5) + 8 <= BAR_BYTES, "barriers fit their block");
+  static_assert(STG_REGION / kPatchStageMax >= 4, "at least four staged blocks of the largest size");
 };
 
-constexpr int kPatchThreads = 320;
+// Staged image blocks ([oh_l][g][x], x over the image width): each at a 1 KB
+// boundary, as many as the region holds (up to 8).
+struct StgRing {
+  uint32_t stride;
+  int n;
+  __device__ __forceinline__ explicit StgRing(uint32_t bytes)
+      : stride((bytes + 1023u) & ~1023u), n(min(PatchLayout::STG_BUFS, (int)(PatchLayout::STG_REGION / stride))) {}
+};
+
+constexpr int kPatchThreads = 352;
 constexpr int kPatchBuilders = 128;  // warps 6..9
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
-// K-major tile (rows of 64 bf16).
-__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Builds tile row r (one output position, or zeros past the tile's positions)
-// of K block `kb` from the staged image rows: chunk 2g+h holds kw = 8h .. 8h+7
-// of kernel row kh0 + g.  Staged layout: [oh_l][g][x], x over the image width.
-__device__ __forceinline__ void build_patch_row(const PatchParams& p, uint32_t a_dst, uint32_t stg,
-                                                int r) {
-  uint32_t v[8][4];
+// Patch-tile row r (one output position; zeros past the tile's positions) of
+// one K block from the staged image rows, as the 32 TMEM columns of the
+// position's lane: column 8g + e holds kw = 2e (low half) and 2e + 1 (high
+// half) of kernel row kh0 + g.
+__device__ __forceinline__ void build_patch_words(const PatchParams& p, uint32_t stg, int r, uint32_t (&v)[32]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) v[c][0] = v[c][1] = v[c][2] = v[c][3] = 0u;
-  if (r < p.tile_rows) {
-    const int oh_l = r / p.Wo;
-    const int ow = r - oh_l * p.Wo;
-    if ((p.KW & 1) == 0) {
-      // Even KW: every staged pair (kw, kw+1) with kw < KW is 4-byte aligned
-      // and lies inside its image row; pairs past KW are not read.
+  for (int c = 0; c < 32; ++c) v[c] = 0u;
+  if (r >= p.tile_rows) return;
+  const int oh_l = r / p.Wo;
+  const int ow = r - oh_l * p.Wo;
+  if ((p.KW & 1) == 0) {
+    // Even KW: every staged pair (kw, kw+1) with kw < KW is 4-byte aligned
+    // and lies inside its image row; pairs past KW are not read.
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (2 * e < p.KW) {
-            uint32_t w;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(row + 4 * e));
-            v[2 * g + (e >> 2)][e & 3] = w;
-          }
-      }
-    } else {
+      for (int e = 0; e < 8; ++e)
+        if (2 * e < p.KW) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[8 * g + e]) : "r"(row + 4 * e));
+    }
+  } else {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t row = stg + (uint32_t)(((oh_l * 4 + g) * p.W + ow * p.KW) * 2);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (e < p.KW) {
-            uint16_t h;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(row + 2 * e));
-            v[2 * g + (e >> 3)][(e & 7) >> 1] |= (uint32_t)h << (16 * (e & 1));
-          }
-      }
+      for (int e = 0; e < 16; ++e)
+        if (e < p.KW) {
+          uint16_t h;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(row + 2 * e));
+          v[8 * g + (e >> 1)] |= (uint32_t)h << (16 * (e & 1));
+        }
     }
   }
+}
+
+// Single thread: the tiles' UMMAs, A (the patch tile) from TMEM stage s, B
+// (the filter block) from shared-memory stage s; accumulators alternate.
+__device__ __forceinline__ void patch_mma(uint32_t sB, const PipeBars& bars, uint32_t tmem_base, int first_tile,
+                                          int num_tiles, int k_blocks, int stride, const WaitCtl& w) {
+  using Lay = PatchLayout;
+  const uint32_t kIdesc = idesc_bf16_f32(kBM, kPatchBN, false);
+  uint32_t it = 0;
+  int local = 0;
+  bool ok = true;
+  for (int tile = first_tile; ok && tile < num_tiles; tile += stride, ++local) {
+    const uint32_t buf = local & 1, use = local >> 1;
+    if (use > 0 && !mbar_wait_bounded(bars.tempty(buf), (use - 1) & 1, w.abort, w.status_word, w.limit_ns,
+                                      status_code(6, kSiteMmaTmemEmpty))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t d = tmem_base + buf * kPatchBN;
+    for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+      const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
+      if (!mbar_wait_bounded(bars.full(s), r & 1, w.abort, w.status_word, w.limit_ns,
+                             status_code(6, kSiteMmaFull))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t a = tmem_base + Lay::A_COL + s * (kBK / 2);
+      const uint32_t b = sB + s * Lay::B_BYTES;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) st_shared_v4(a_dst + sw128_chunk(r, c), v[c][0], v[c][1], v[c][2], v[c][3]);
+      for (int k = 0; k < kBK / kUmmaK; ++k)  // one kernel row per step, ascending
+        umma_bf16_ts(d, a + k * (kUmmaK / 2), smem_desc_sw128(b + k * 32, 16, 1024), kIdesc,
+                     (kb | k) != 0 ? 1u : 0u);
+      umma_commit(bars.empty(s));  // filter stage and patch-tile stage s are free once these finish
+    }
+    if (!ok) break;
+    umma_commit(bars.tfull(buf));
+  }
+  // Every MMA issued above has finished before TMEM can be released.
+  umma_commit(bars.drain);
+  mbar_wait_bounded(bars.drain, 0, nullptr, w.status_word, w.limit_ns, status_code(6, kSiteDrain));
 }
 
 __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_constant__ PatchParams p) {
@@ -111,10 +163,10 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sA = base;
-  const uint32_t sB = sA + Lay::STAGES * Lay::A_BYTES;
+  const uint32_t sB = base;
   const uint32_t sStg = sB + Lay::STAGES * Lay::B_BYTES;
-  const uint32_t bar0 = sStg + Lay::STG_BUFS * kPatchStageMax;
+  const uint32_t bar0 = sStg + Lay::STG_REGION;
+  const StgRing ring(p.stg_bytes);
   PipeBars bars;
   bars.full0 = bar0;
   bars.empty0 = bar0 + 8 * Lay::STAGES;
@@ -131,12 +183,12 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     // A stage is full when its filter block has landed and the four builder
-    // warps have written its patch tile.
+    // warps have written its patch tile into TMEM.
     for (int s = 0; s < Lay::STAGES; ++s) {
       mbar_init(bars.full(s), 1 + kPatchBuilders / 32);
       mbar_init(bars.empty(s), 1);
     }
-    for (int q = 0; q < Lay::STG_BUFS; ++q) {
+    for (int q = 0; q < ring.n; ++q) {
       mbar_init(stg_full0 + 8 * q, 1);
       mbar_init(stg_empty0 + 8 * q, kPatchBuilders / 32);
     }
@@ -168,24 +220,13 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
         const TileCoord tc = decode_tile(tile, p.m_tiles, p.n_tiles);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
-          const uint32_t q = it % Lay::STG_BUFS, rq = it / Lay::STG_BUFS;
           if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
                                           wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
             ok = false;
             break;
           }
-          if (rq > 0 && !mbar_wait_bounded(stg_empty0 + 8 * q, (rq - 1) & 1, wc.abort, wc.status_word,
-                                           wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
-            ok = false;
-            break;
-          }
           mbar_arrive_expect_tx(bars.full(s), Lay::B_BYTES);
-          tma_load_3d(sB + s * Lay::B_BYTES, &p.tma_w, bars.full(s), kb * kBK, tc.nb * kBN, 0);
-          const int ci = kb / p.khq;
-          const int kh0 = (kb - ci * p.khq) * 4;
-          mbar_arrive_expect_tx(stg_full0 + 8 * q, p.stg_bytes);
-          tma_load_4d(sStg + q * kPatchStageMax, &p.tma_x, stg_full0 + 8 * q, 0, kh0, tc.mb * p.t_oh,
-                      tc.l * p.C + ci);
+          tma_load_3d(sB + s * Lay::B_BYTES, &p.tma_w, bars.full(s), kb * kBK, tc.nb * kPatchBN, 0);
         }
       }
       // No copy may still be landing in shared memory when the CTA exits.
@@ -194,16 +235,35 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
         if (!mbar_wait_bounded(bars.full(j % Lay::STAGES), (j / Lay::STAGES) & 1, nullptr,
                                wc.status_word, wc.limit_ns, status_code(6, kSiteDrain)))
           break;
-      const uint32_t first_q = it > (uint32_t)Lay::STG_BUFS ? it - Lay::STG_BUFS : 0u;
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(tile, p.m_tiles, p.n_tiles);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const uint32_t q = it % ring.n, rq = it / ring.n;
+          if (rq > 0 && !mbar_wait_bounded(stg_empty0 + 8 * q, (rq - 1) & 1, wc.abort, wc.status_word,
+                                           wc.limit_ns, status_code(6, kSiteProducerEmpty))) {
+            ok = false;
+            break;
+          }
+          const int ci = kb / p.khq;
+          const int kh0 = (kb - ci * p.khq) * 4;
+          mbar_arrive_expect_tx(stg_full0 + 8 * q, p.stg_bytes);
+          tma_load_4d(sStg + q * ring.stride, &p.tma_x, stg_full0 + 8 * q, 0, kh0, tc.mb * p.t_oh,
+                      tc.l * p.C + ci);
+        }
+      }
+      const uint32_t first_q = it > (uint32_t)ring.n ? it - ring.n : 0u;
       for (uint32_t j = first_q; j < it; ++j)
-        if (!mbar_wait_bounded(stg_full0 + 8 * (j % Lay::STG_BUFS), (j / Lay::STG_BUFS) & 1, nullptr,
-                               wc.status_word, wc.limit_ns, status_code(6, kSiteDrain)))
+        if (!mbar_wait_bounded(stg_full0 + 8 * (j % ring.n), (j / ring.n) & 1, nullptr, wc.status_word,
+                               wc.limit_ns, status_code(6, kSiteDrain)))
           break;
     }
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role<Lay::STAGES, Lay::A_BYTES, Lay::B_BYTES, false>(
-          sA, sB, bars, tmem_base, blockIdx.x, p.num_tiles, p.k_blocks, gridDim.x, wc);
+    if (lane == 0) patch_mma(sB, bars, tmem_base, blockIdx.x, p.num_tiles, p.k_blocks, gridDim.x, wc);
   } else if (warp < 6) {
     OutDesc o;
     o.c = p.y;
@@ -223,17 +283,19 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
     o.trans = 1;
     o.tile_rows = p.tile_rows;
     o.out_f16 = 0;
-    epilogue_role(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles, p.n_tiles,
-                  gridDim.x, o, 0u, wc);
-  } else {
-    // Patch-tile builders: thread t writes tile row t of every K block.
-    const int t = threadIdx.x - 6 * 32;
+    epilogue_role<false, kPatchBN, 2>(warp & 3, lane, tmem_base, bars, blockIdx.x, p.num_tiles, p.m_tiles,
+                                      p.n_tiles, gridDim.x, o, 0u, wc);
+  } else if (warp < 10) {
+    // Patch-tile builders: a warp may reach only its TMEM lane quadrant, so
+    // thread `lane` of warp w writes tile row 32 (w % 4) + lane.
+    const int t = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + Lay::A_COL;
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
         const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
-        const uint32_t q = it % Lay::STG_BUFS, rq = it / Lay::STG_BUFS;
+        const uint32_t q = it % ring.n, rq = it / ring.n;
         bool got = mbar_wait_bounded(stg_full0 + 8 * q, rq & 1, wc.abort, wc.status_word, wc.limit_ns,
                                      status_code(6, kSiteConvProducer));
         if (got && r > 0)
@@ -243,8 +305,12 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
           ok = false;
           break;
         }
-        build_patch_row(p, sA + s * Lay::A_BYTES, sStg + q * kPatchStageMax, t);
-        fence_proxy_async_smem();
+        tc_fence_after_sync();  // the MMAs that read patch stage s have finished
+        uint32_t v[32];
+        build_patch_words(p, sStg + q * ring.stride, t, v);
+        tmem_store_32cols(lane_base + s * (kBK / 2), v);
+        tmem_store_wait();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(bars.full(s));
@@ -288,6 +354,14 @@ __global__ void conv_pack_kernel(const uint16_t* __restrict__ w, uint16_t* __res
 
 int64_t patch_padded_k(int64_t C, int64_t KH) { return C * ((KH + 3) / 4 * 4) * 16; }
 
+int64_t patch_stage_bytes(int64_t W, int64_t t_oh) { return W * 4 * t_oh * 2; }
+
+int64_t patch_tile_rows(int64_t Ho, int64_t Wo, int64_t W) {
+  int64_t t = std::min<int64_t>(Ho, kBM / std::max<int64_t>(Wo, 1));
+  while (t > 1 && patch_stage_bytes(W, t) > kPatchStageMax) --t;
+  return std::max<int64_t>(t, 1);
+}
+
 bi_status launch_conv_pack(const void* w, void* dst, int64_t Co, int64_t C, int64_t KH, int64_t KW,
                            cudaStream_t stream, std::string* why) {
   DeviceInfo dev;
@@ -314,7 +388,7 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
   PatchParams p;
   memset(&p, 0, sizeof(p));
   const int64_t Kp = patch_padded_k(pp.C, pp.KH);
-  const int64_t t_oh = std::min<int64_t>(pp.Ho, kBM / pp.Wo);
+  const int64_t t_oh = patch_tile_rows(pp.Ho, pp.Wo, pp.W);
   // x as {W, KH, Ho, B*C}: element (x, kh, oh, b*C + ci) is x[b][ci][oh*KH + kh][x].
   {
     const cuuint64_t dims[4] = {(cuuint64_t)pp.W, (cuuint64_t)pp.KH, (cuuint64_t)pp.Ho,
@@ -329,7 +403,7 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
   {
     const cuuint64_t dims[3] = {(cuuint64_t)Kp, (cuuint64_t)pp.Co, 1};
     const cuuint64_t strides[2] = {(cuuint64_t)Kp * 2, (cuuint64_t)(Kp * 2 * pp.Co)};
-    const cuuint32_t box[3] = {kBK, kBN, 1};
+    const cuuint32_t box[3] = {kBK, kPatchBN, 1};
     if (!encode_tiled_bf16(&p.tma_w, const_cast<void*>(pp.wp), 3, dims, strides, box, why))
       return BI_ERR_CUDA;
   }
@@ -345,7 +419,7 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
   p.P = (int32_t)(pp.Ho * pp.Wo);
   p.Co = (int32_t)pp.Co;
   p.m_tiles = (int32_t)((pp.Ho + t_oh - 1) / t_oh);
-  p.n_tiles = (int32_t)((pp.Co + kBN - 1) / kBN);
+  p.n_tiles = (int32_t)((pp.Co + kPatchBN - 1) / kPatchBN);
   p.k_blocks = (int32_t)(Kp / kBK);
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles * pp.B;
   if (tiles > INT32_MAX) {
