@@ -278,11 +278,22 @@ def time_launch(fn, flush_buf, stream):
     return e0, e1
 
 
+def trimmed_mean(ts) -> float:
+    """Mean of the samples without the top and bottom tenth (at least one each
+    when there are five or more).  The device timer behind CUDA events ticks in
+    steps of about 1-2 us here, so a single launch of a 10-30 us kernel reads a
+    whole number of ticks; averaging launches whose start falls at different
+    points of a tick recovers the duration, which a median cannot."""
+    ts = sorted(ts)
+    k = max(1, len(ts) // 10) if len(ts) >= 5 else 0
+    ts = ts[k:len(ts) - k]
+    return sum(ts) / len(ts)
+
+
 def measure(fn, flush_buf, stream, reps: int) -> float:
     evs = [time_launch(fn, flush_buf, stream) for _ in range(reps)]
     torch.cuda.synchronize()
-    ts = sorted(a.elapsed_time(b) * 1e-3 for a, b in evs)
-    return ts[len(ts) // 2]
+    return trimmed_mean([a.elapsed_time(b) * 1e-3 for a, b in evs])
 
 
 def bits_equal(x, y) -> bool:
@@ -624,7 +635,7 @@ def run_ours(args, rank, local, world):
 
     sweep = []
     for M in Ms:
-        t = statistics.median(per_m[M])
+        t = trimmed_mean(per_m[M])
         frac, bound = roofline_frac(addmm_flops(M), addmm_bytes(M), t, peaks)
         sweep.append({"M": M, "us": round(t * 1e6, 2), "tflops": round(addmm_flops(M) / t / 1e12, 2),
                       "gbs": round(addmm_bytes(M) / t / 1e9, 1), "roofline_frac": round(frac, 3),
