@@ -72,6 +72,7 @@ PATCH_CASES = [
     (1, 2, 33, 64, 16, 5, 3, torch.float32, None),                   # leftover rows and columns
     (2, 3, 32, 256, 64, 2, 2, torch.bfloat16, torch.float32),        # widest image, 128 patches a row
     (1, 3, 64, 64, 300, 16, 16, torch.bfloat16, None),
+    (1, 3, 224, 224, 1153, 14, 14, torch.float32, torch.bfloat16),  # 6 whole 192-channel tiles + 1 channel
 ]
 
 

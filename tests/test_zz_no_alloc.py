@@ -63,3 +63,20 @@ def test_noalloc_equals_caller_workspace_bit_for_bit():
     assert binding.bi_attention_workspace_bytes(L, Tq2, 6000) <= SCRATCH
     assert bits_equal(binding.bi_attention_noalloc(q2, k2, v2, 0.0625), binding.bi_attention_ws(q2, k2, v2, 0.0625))
     assert binding.bi_device_status() == binding.BI_OK
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d", [64, 128])
+def test_noalloc_narrow_heads_equal_caller_workspace(d):
+    # the scratch holds ceil(Tk / 2048) * L * Tq * (d + 2) floats for a narrower head
+    binding.load()
+    L, Tq, Tk = 3, 260, 4500
+    need = binding.bi_attention_workspace_bytes(L, Tq, Tk, d)
+    assert need == 3 * L * Tq * (d + 2) * 4 and need <= SCRATCH
+    q = inputs.normal_bf16((L, Tq, d), 1.0, 76).cuda()
+    k = inputs.normal_bf16((L, Tk, d), 1.0, 77).cuda()
+    v = inputs.normal_bf16((L, Tk, d), 1.0, 78).cuda()
+    for od in (torch.float32, torch.bfloat16):
+        assert bits_equal(binding.bi_attention_noalloc(q, k, v, d ** -0.5, out_dtype=od),
+                          binding.bi_attention_ws(q, k, v, d ** -0.5, out_dtype=od))
+    assert binding.bi_device_status() == binding.BI_OK
