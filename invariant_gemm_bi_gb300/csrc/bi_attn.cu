@@ -29,10 +29,11 @@
 // ring of 128 KB of stages), 1 MMA issuer (one thread), 2-9 softmax and
 // epilogue: warps w and w + 4 share the 32 query rows of TMEM lane quadrant
 // w % 4, one row per thread; warps 2-5 take keys 0-63 of each block and O
-// columns 0-127, warps 6-9 keys 64-127 and O columns 128-255.  The two warps
-// of a quadrant exchange their block maxima through a TMEM column of the S
-// buffer they have consumed, write their halves of the bf16 P row back into
-// that buffer (keys 64h.. at columns 64h..64h+31), and decide every wait
+// columns 0-127, warps 6-9 keys 64-127 and O columns 128-255 (for D = 256;
+// O columns D/2 h.. in general).  The two warps of a quadrant exchange their
+// block maxima through shared memory, write their halves of the bf16 P row
+// back into the S buffer they have consumed (keys 64h.. at columns
+// 64h..64h+31), and decide every wait
 // together (a barrier that ANDs their outcomes), so they always take the same
 // path.  The tensor core runs one thread's MMAs in issue order, so S_{j+2}
 // (issued after PV_j) never overwrites P_j before PV_j has read it, and the
@@ -410,14 +411,13 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         for (int i = 8; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], t[i]);
         mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       }
-      // Exchange the halves' maxima through the last column of each half of
-      // the consumed S buffer (P takes the first 32 columns of each half).
-      tmem_store_1col(scol + 63, __float_as_uint(mx));
-      tmem_store_wait();
-      tc_fence_before_sync();
+      // Exchange the halves' maxima through shared memory (the running-sum
+      // exchange area, slot hc of the row).  A slot is written again only
+      // after a later barrier of the pair: the P signal wait of this block,
+      // or the one below for the first block.
+      xch[hc * kAttnBM + row] = mx;
       named_barrier(pair_bar, 64);
-      tc_fence_after_sync();
-      const float mo = __uint_as_float(tmem_load_1col(trow + buf * kAttnBN + (1 - hc) * 64 + 63));
+      const float mo = xch[(1 - hc) * kAttnBM + row];
       ++sc;
       const float m_blk = hc == 0 ? fmaxf(mx, mo) : fmaxf(mo, mx);  // the same operands in both warps
       const float m_new = fmaxf(m, m_blk);
@@ -478,6 +478,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, const AttnBars
         ok = false;
         break;
       }
+      if (pc == 0) named_barrier(pair_bar, 64);  // the partner has read this block's maximum
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.p_full());
       ++pc;

@@ -36,18 +36,6 @@ __device__ __forceinline__ void tmem_store_32cols(uint32_t taddr, const uint32_t
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-// One fp32 column of 32 lanes: thread t of the warp reads / writes row (lane
-// base + t) of column col.
-__device__ __forceinline__ uint32_t tmem_load_1col(uint32_t taddr) {
-  uint32_t r;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r)::"memory");
-  return r;
-}
-__device__ __forceinline__ void tmem_store_1col(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 // A float at the shared::cluster address `addr` (from cluster_map_shared).
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
