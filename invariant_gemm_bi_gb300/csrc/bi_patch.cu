@@ -20,8 +20,8 @@
 // builder warps then turn the staged rows into the patch tile (one row per
 // output position, zeros for kw >= KW) and write it straight into tensor
 // memory, where the MMA takes its A operand: the tile never passes through
-// shared memory, whose bandwidth (image rows in and out, filter in and out)
-// is what bounds this kernel.  A tile is (sample, block of t_oh output rows,
+// shared memory (writing and reading it there was the largest share of the
+// shared-memory traffic).  A tile is (sample, block of t_oh output rows,
 // 192 channels): it never mixes samples, so one sample's arithmetic is the
 // same for every batch size.
 //
