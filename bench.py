@@ -280,10 +280,8 @@ def time_launch(fn, flush_buf, stream):
 
 def trimmed_mean(ts) -> float:
     """Mean of the samples without the top and bottom tenth (at least one each
-    when there are five or more).  The device timer behind CUDA events ticks in
-    steps of about 1-2 us here, so a single launch of a 10-30 us kernel reads a
-    whole number of ticks; averaging launches whose start falls at different
-    points of a tick recovers the duration, which a median cannot."""
+    when there are five or more): every launch counts, a stray slow or fast
+    one does not."""
     ts = sorted(ts)
     k = max(1, len(ts) // 10) if len(ts) >= 5 else 0
     ts = ts[k:len(ts) - k]
