@@ -10,8 +10,8 @@
 // Work unit: one head l and 128 consecutive query rows (a tile); a persistent
 // CTA takes tiles c, c + grid, ...  Per tile, for key blocks j = 0, 1, ... of
 // 128 keys in ascending order:
-//   S_j  = q k_j^T                    tcgen05.mma 128 x 128 x 16, 16 steps over D
-//                                      ascending, fp32 in TMEM (two S buffers)
+//   S_j  = q k_j^T                    tcgen05.mma 128 x 128 x 16, D / 16 steps
+//                                      over D ascending, fp32 in TMEM (two S buffers)
 //   t    = RN(S_j * c),  c = RN(scale * log2 e);  keys >= Tk -> -inf
 //   m    = running row maximum of t, kept unless a block raises it by more
 //          than 8 (then O and the running sum are rescaled by 2^(m_old - m_new))
@@ -19,7 +19,7 @@
 //   l_h  = RN(l_h * alpha) + ((a0 + a1) + (a2 + a3)) for each half h of the
 //          block (keys 0-63, 64-127), a_r the sum of the half's p with key
 //          index = r mod 4, ascending;  l = l_0 + l_1 at the end
-//   O   += bf16(p) v_j                tcgen05.mma 128 x 256 x 16, keys ascending,
+//   O   += bf16(p) v_j                tcgen05.mma 128 x D x 16, keys ascending,
 //                                      P read from TMEM, fp32 O in TMEM
 // and finally o = RN(O * RN(1 / l)), rounded once to the output type.  Every
 // step is a function of the query row, the head's keys and values, Tk and
