@@ -278,20 +278,33 @@ def time_launch(fn, flush_buf, stream):
     return e0, e1
 
 
-def trimmed_mean(ts) -> float:
-    """Mean of the samples without the top and bottom tenth (at least one each
-    when there are five or more): every launch counts, a stray slow or fast
-    one does not."""
+def quantile(ts, q: float) -> float:
+    """Linear-interpolated quantile q (0..1) of the samples."""
     ts = sorted(ts)
-    k = max(1, len(ts) // 10) if len(ts) >= 5 else 0
-    ts = ts[k:len(ts) - k]
-    return sum(ts) / len(ts)
+    if len(ts) == 1:
+        return ts[0]
+    x = q * (len(ts) - 1)
+    i = int(x)
+    j = min(i + 1, len(ts) - 1)
+    return ts[i] + (ts[j] - ts[i]) * (x - i)
+
+
+def spread(ts) -> dict:
+    """Median and the 10th / 90th percentiles of per-launch times (seconds), in µs."""
+    return {"p10_us": round(quantile(ts, 0.1) * 1e6, 2), "p90_us": round(quantile(ts, 0.9) * 1e6, 2),
+            "launches": len(ts)}
+
+
+def measure_all(fn, flush_buf, stream, reps: int) -> list[float]:
+    """Per-launch times (seconds) of `reps` launches, each after an L2 flush."""
+    evs = [time_launch(fn, flush_buf, stream) for _ in range(reps)]
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in evs]
 
 
 def measure(fn, flush_buf, stream, reps: int) -> float:
-    evs = [time_launch(fn, flush_buf, stream) for _ in range(reps)]
-    torch.cuda.synchronize()
-    return trimmed_mean([a.elapsed_time(b) * 1e-3 for a, b in evs])
+    """Median per-launch time (seconds)."""
+    return statistics.median(measure_all(fn, flush_buf, stream, reps))
 
 
 def bits_equal(x, y) -> bool:
@@ -315,7 +328,7 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -
     if want("attention"):
         _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
     if want("tiny"):
-        _tiny(out, binding, inputs, flush_buf, stream, reps)
+        _tiny(out, binding, inputs, flush_buf, stream, 20 * reps)  # >= 1000 launches per point at reps >= 50
     if want("fp16"):
         _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
     if want("rows"):
@@ -324,10 +337,17 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -
 
 
 def point_fn(peaks):
+    """point(flops, bytes, t): figures at the median of t (a list of per-launch
+    times, or one time), with the 10th / 90th percentiles of a list."""
     def point(flops, nbytes, t):
-        frac, bound = roofline_frac(flops, nbytes, t, peaks)
-        return {"us": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 2),
-                "gbs": round(nbytes / t / 1e9, 1), "roofline_frac": round(frac, 3), "bound": bound}
+        ts = t if isinstance(t, list) else [t]
+        med = statistics.median(ts)
+        frac, bound = roofline_frac(flops, nbytes, med, peaks)
+        d = {"us": round(med * 1e6, 2), "tflops": round(flops / med / 1e12, 2),
+             "gbs": round(nbytes / med / 1e9, 1), "roofline_frac": round(frac, 3), "bound": bound}
+        if len(ts) > 1:
+            d.update(spread(ts))
+        return d
     return point
 
 
@@ -340,8 +360,8 @@ def _square(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         am = a[:M]
         c = torch.empty(M, 8192, dtype=torch.float32, device="cuda")
         cp = torch.empty(M, 8192, dtype=torch.float32, device="cuda")
-        t = measure(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
-        tp = measure(lambda: binding.bi_addmm_packed(None, am, wp, out=cp), flush_buf, stream, reps)
+        t = measure_all(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
+        tp = measure_all(lambda: binding.bi_addmm_packed(None, am, wp, out=cp), flush_buf, stream, reps)
         rows0[M] = c[:1].clone()
         flops, nb = 2.0 * M * 8192 * 8192, 2.0 * (M * 8192 + 8192 * 8192) + 4.0 * M * 8192
         r = {"M": M, **point(flops, nb, t),
@@ -370,7 +390,7 @@ def _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point):
     for M in inputs.LLM_ADDMM_F16_M:
         xm = x[:M]
         c = torch.empty(M, N_DIM, dtype=torch.float16, device="cuda")
-        t = measure(lambda: binding.bi_addmm_packed(bias, xm, wp, out=c), flush_buf, stream, reps)
+        t = measure_all(lambda: binding.bi_addmm_packed(bias, xm, wp, out=c), flush_buf, stream, reps)
         rows0[M] = c[:1].clone()
         r = {"M": M, **point(addmm_flops(M), addmm_bytes(M), t)}
         r["cublas_us"] = round(measure(lambda: torch.addmm(bias, xm, w), flush_buf, stream, reps) * 1e6, 2)
@@ -391,12 +411,12 @@ def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
     for B in inputs.PATCH_EMBED_B:
         xb = x[:B]
         y = torch.empty(B, 1152, 16, 16, dtype=torch.bfloat16, device="cuda")
-        t = measure(lambda: binding.bi_conv2d_patch_packed(xb, wpk, bc, out=y), flush_buf, stream, reps)
+        t = measure_all(lambda: binding.bi_conv2d_patch_packed(xb, wpk, bc, out=y), flush_buf, stream, reps)
         y0[B] = y[:1].clone()
         flops = B * (2.0 * 256 * 588 * 1152 + 256 * 1152)
         nb = 2.0 * (B * 3 * 224 * 224 + 1152 * 588 + 1152 + B * 1152 * 256)
         r = {"B": B, **point(flops, nb, t)}
-        tp = measure(lambda: binding.bi_conv2d_patch(xb, wc, bc, stride=14, out=y), flush_buf, stream, reps)
+        tp = measure_all(lambda: binding.bi_conv2d_patch(xb, wc, bc, stride=14, out=y), flush_buf, stream, reps)
         yp0[B] = y[:1].clone()
         r["plain_filter"] = point(flops, nb, tp)
         tc = measure(lambda: F.conv2d(xb, wc, bc, stride=14), flush_buf, stream, reps)
@@ -422,10 +442,11 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         s = torch.empty(L, 816, 816, dtype=torch.float32, device="cuda")
         p = torch.empty(L, 816, 816, dtype=torch.bfloat16, device="cuda")
         o = torch.empty(L, 816, 256, dtype=torch.float32, device="cuda")
-        t1 = measure(lambda: binding.bi_bmm(qb, kb, alpha=1.0 / 16, out=s), flush_buf, stream, reps)
-        t2 = measure(lambda: binding.bi_softmax_lastdim(s.view(-1, 816), out=p.view(-1, 816)),
-                     flush_buf, stream, reps)
-        t3 = measure(lambda: binding.bi_bmm(p, vb, out=o), flush_buf, stream, reps)
+        t1 = measure_all(lambda: binding.bi_bmm(qb, kb, alpha=1.0 / 16, out=s), flush_buf, stream, reps)
+        t2s = measure_all(lambda: binding.bi_softmax_lastdim(s.view(-1, 816), out=p.view(-1, 816)),
+                          flush_buf, stream, reps)
+        t2 = statistics.median(t2s)
+        t3 = measure_all(lambda: binding.bi_bmm(p, vb, out=o), flush_buf, stream, reps)
         o0[B] = o[:1].clone()
         f1 = L * 2.0 * 816 * 816 * 256
         b1 = L * (2.0 * 816 * 256 * 2 + 4.0 * 816 * 816)
@@ -434,7 +455,7 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         tcb = measure(lambda: torch.bmm(qb, kb), flush_buf, stream, reps)
         # the same attention fused in one kernel (fp32 out), and PyTorch's SDPA
         of = torch.empty(L, 816, 256, dtype=torch.float32, device="cuda")
-        tf = measure(lambda: binding.bi_attention(qb, k[:L], vb, 1.0 / 16, out=of), flush_buf, stream, reps)
+        tf = measure_all(lambda: binding.bi_attention(qb, k[:L], vb, 1.0 / 16, out=of), flush_buf, stream, reps)
         of0[B] = of[:1].clone()
         ff = 2 * f1
         bf = L * (3 * 2.0 * 816 * 256 + 4.0 * 816 * 256)
@@ -445,7 +466,8 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         del of
         res.append({"B": B, "fused": fused, "qk": point(f1, b1, t1),
                     "softmax": {"us": round(t2 * 1e6, 2), "gbs": round(b2 / t2 / 1e9, 1),
-                                "roofline_frac": round(b2 / (peaks["hbm_gbs"] * 1e9) / t2, 3), "bound": "hbm"},
+                                "roofline_frac": round(b2 / (peaks["hbm_gbs"] * 1e9) / t2, 3), "bound": "hbm",
+                                **spread(t2s)},
                     "pv": point(f1, b3, t3), "cublas_qk_us": round(tcb * 1e6, 2)})
         del s, p, o
     # a long key range: one sample (8 heads), T = 8192 -- fused with four fixed
@@ -456,8 +478,8 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
     bl = Lh * (3 * 2.0 * T * 256 + 4.0 * T * 256)
     ol = torch.empty(Lh, T, 256, dtype=torch.float32, device="cuda")
     ws = torch.empty(binding.bi_attention_workspace_bytes(Lh, T, T), dtype=torch.uint8, device="cuda")
-    tfl = measure(lambda: binding.bi_attention_ws(ql, kl, vl, 1.0 / 16, out=ol, workspace=ws), flush_buf, stream,
-                  reps)
+    tfl = measure_all(lambda: binding.bi_attention_ws(ql, kl, vl, 1.0 / 16, out=ol, workspace=ws), flush_buf,
+                      stream, reps)
     sl = torch.empty(Lh, T, T, dtype=torch.float32, device="cuda")
     pl = torch.empty(Lh, T, T, dtype=torch.bfloat16, device="cuda")
     oc = torch.empty(Lh, T, 256, dtype=torch.float32, device="cuda")
@@ -483,7 +505,7 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         qd, kd, vd = inputs.attention(32, d=d, device="cuda")
         Ld = qd.shape[0]
         od = torch.empty(Ld, 816, d, dtype=torch.bfloat16, device="cuda")
-        td = measure(lambda: binding.bi_attention(qd, kd, vd, d ** -0.5, out=od), flush_buf, stream, reps)
+        td = measure_all(lambda: binding.bi_attention(qd, kd, vd, d ** -0.5, out=od), flush_buf, stream, reps)
         tsd = measure(lambda: torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, scale=d ** -0.5),
                       flush_buf, stream, reps)
         fd = 4.0 * Ld * 816 * 816 * d
@@ -503,9 +525,11 @@ def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
     # mean of [R, 4096] bf16 (fp32 out); PyTorch's own kernels alongside
     hbm = peaks["hbm_gbs"] * 1e9
 
-    def pt(nb, t, t_torch):
+    def pt(nb, ts, t_torch):
+        t = statistics.median(ts)
         return {"us": round(t * 1e6, 2), "gbs": round(nb / t / 1e9, 1),
-                "roofline_frac": round(nb / hbm / t, 3), "bound": "hbm", "torch_us": round(t_torch * 1e6, 2)}
+                "roofline_frac": round(nb / hbm / t, 3), "bound": "hbm", "torch_us": round(t_torch * 1e6, 2),
+                **spread(ts)}
 
     x, w = inputs.rmsnorm_hidden(max(inputs.RMSNORM_ROWS), device="cuda")
     s = inputs.vocab_logits(max(inputs.LOGITS_ROWS), device="cuda")
@@ -515,10 +539,10 @@ def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
         xr = x[:R]
         y = torch.empty(R, N, dtype=torch.bfloat16, device="cuda")
         m = torch.empty(R, dtype=torch.float32, device="cuda")
-        t = measure(lambda: binding.bi_rmsnorm_lastdim(xr, w, 1e-6, out=y), flush_buf, stream, reps)
+        t = measure_all(lambda: binding.bi_rmsnorm_lastdim(xr, w, 1e-6, out=y), flush_buf, stream, reps)
         tt = measure(lambda: torch.nn.functional.rms_norm(xr, (N,), w, 1e-6), flush_buf, stream, reps)
         rms.append({"rows": R, **pt(2.0 * (2 * R * N + N), t, tt)})
-        tm = measure(lambda: binding.bi_mean_lastdim(xr, out=m), flush_buf, stream, reps)
+        tm = measure_all(lambda: binding.bi_mean_lastdim(xr, out=m), flush_buf, stream, reps)
         ttm = measure(lambda: torch.mean(xr, dim=-1, dtype=torch.float32), flush_buf, stream, reps)
         mean.append({"rows": R, **pt(2.0 * R * N + 4.0 * R, tm, ttm)})
         r0["rms"][R], r0["mean"][R] = y[:1].clone(), m[:1].clone()
@@ -526,7 +550,7 @@ def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
     for R in inputs.LOGITS_ROWS:
         sr = s[:R]
         y = torch.empty(R, V, dtype=torch.float32, device="cuda")
-        t = measure(lambda: binding.bi_log_softmax_lastdim(sr, out=y), flush_buf, stream, reps)
+        t = measure_all(lambda: binding.bi_log_softmax_lastdim(sr, out=y), flush_buf, stream, reps)
         tt = measure(lambda: torch.log_softmax(sr, dim=-1), flush_buf, stream, reps)
         lsm.append({"rows": R, **pt(8.0 * R * V, t, tt)})
         r0["lsm"][R] = y[:1].clone()
@@ -539,15 +563,23 @@ def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
 
 
 def _tiny(out, binding, inputs, flush_buf, stream, reps):
-    # launch-latency bound: report microseconds
+    # launch-latency bound: report microseconds (median over `reps` launches,
+    # each after an L2 flush), cuBLAS (fp32 out) on the same shapes alongside
     a, w = inputs.tiny_mm(64, device="cuda")
-    res = []
+    res, rows0, cub0 = [], {}, {}
     for M in inputs.TINY_MM_M:
         am = a[:M]
         c = torch.empty(M, 128, dtype=torch.float32, device="cuda")
-        t = measure(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
-        res.append({"M": M, "us": round(t * 1e6, 2)})
-    out["tiny_mm"] = {"points": res}
+        cb = torch.empty(M, 128, dtype=torch.bfloat16, device="cuda")
+        ts = measure_all(lambda: binding.bi_mm(am, w, out=c), flush_buf, stream, reps)
+        rows0[M] = c[:1].clone()
+        tc = measure_all(lambda: torch.mm(am, w, out=cb), flush_buf, stream, reps)
+        cub0[M] = torch.mm(am, w)[:1].clone()
+        res.append({"M": M, "us": round(statistics.median(ts) * 1e6, 2), **spread(ts),
+                    "cublas_us_bf16_out": round(statistics.median(tc) * 1e6, 2)})
+    out["tiny_mm"] = {"points": res,
+                      "row0_bit_equal_all_M": all(bits_equal(rows0[M], rows0[1]) for M in rows0),
+                      "cublas_row0_bit_equal_all_M": all(bits_equal(cub0[M], cub0[1]) for M in cub0)}
 
 
 def run_only(args):
@@ -631,20 +663,15 @@ def run_ours(args, rank, local, world):
     value = total_flops / kernel_s / 1e12
     gpu_launches = len(Ms) * args.steps
 
-    sweep = []
-    for M in Ms:
-        t = trimmed_mean(per_m[M])
-        frac, bound = roofline_frac(addmm_flops(M), addmm_bytes(M), t, peaks)
-        sweep.append({"M": M, "us": round(t * 1e6, 2), "tflops": round(addmm_flops(M) / t / 1e12, 2),
-                      "gbs": round(addmm_bytes(M) / t / 1e9, 1), "roofline_frac": round(frac, 3),
-                      "bound": bound})
+    point = point_fn(peaks)
+    sweep = [{"M": M, **point(addmm_flops(M), addmm_bytes(M), per_m[M])} for M in Ms]
 
     # the other weight path, same shapes
     other_out = {M: torch.empty(M, N_DIM, dtype=torch.bfloat16, device="cuda") for M in Ms}
     other_name = "plain_weight_us" if args.weight == "packed" else "packed_weight_us"
     for r in sweep:
         M = r["M"]
-        r[other_name] = round(measure(lambda: other_fn(M, other_out[M]), flush_buf, stream, 5) * 1e6, 2)
+        r[other_name] = round(measure(lambda: other_fn(M, other_out[M]), flush_buf, stream, 20) * 1e6, 2)
     del other_out
 
     # cuBLAS on the same sweep (not invariant in general): time + row-0 flag
@@ -652,14 +679,15 @@ def run_ours(args, rank, local, world):
     if not args.no_compare:
         cub = {}
         for M in Ms:
-            tcb = measure(lambda: torch.addmm(bias, xs[M], w), flush_buf, stream, 5)
+            tcb = measure(lambda: torch.addmm(bias, xs[M], w), flush_buf, stream, 20)
             cub[M] = (tcb, torch.addmm(bias, xs[M], w)[:1].clone())
         for r in sweep:
             r["cublas_us"] = round(cub[r["M"]][0] * 1e6, 2)
         cublas_row0 = all(bits_equal(cub[M][1], cub[Ms[0]][1]) for M in Ms)
 
-    # dominant kernel: the M=8192 launch of gemm_kernel
-    t_dom = statistics.mean(per_m[M_max])
+    # dominant kernel: the M=8192 launch of gemm_kernel, at the median launch
+    # time (the statistic of every sweep point)
+    t_dom = statistics.median(per_m[M_max])
     f_dom = addmm_flops(M_max)
     traffic = load_traffic()
     roof = {"bound": "tensor", "achieved": round(f_dom / t_dom / 1e12, 2),
@@ -716,7 +744,7 @@ def run_ours(args, rank, local, world):
 
     sweeps = None
     if not args.headline_only and not args.m_list:
-        sweeps = extra_sweeps(flush_buf, stream, peaks, reps=max(3, min(args.steps, 10)))
+        sweeps = extra_sweeps(flush_buf, stream, peaks, reps=args.sweep_reps)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -733,7 +761,8 @@ def run_ours(args, rank, local, world):
                                       "plain [4096,14336] weight)" if args.weight == "packed"
                                       else "plain row-major [4096,14336]"),
                            "l2": "flushed before every timed launch: 512 MB written then read back (L2 cold and clean)",
-                           "timing": "CUDA events around each launch on its stream; flush excluded",
+                           "timing": ("CUDA events around each launch on its stream; flush excluded; per point "
+                                      "the median launch with p10 / p90; value = all FLOP / all launch time"),
                            "wall_s_timed_region": round(t_wall, 3)},
                 "row0_bit_equal_all_M": row0_equal,
                 "packed_equals_plain_all_M": packed_equals_plain,
@@ -762,8 +791,10 @@ def main():
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
     ap.add_argument("--only", choices=["square", "conv", "attention", "tiny", "fp16", "rows"], default=None,
                     help="measure only this workload (no headline line; for profiling)")
-    ap.add_argument("--weight", choices=["packed", "plain"], default="packed",
+    ap.add_argument("--weight", choices=["packed", "plain"], default="plain",
                     help="weight path of the timed step (the other one is measured alongside)")
+    ap.add_argument("--sweep-reps", type=int, default=50,
+                    help="launches per point of the other workloads (tiny mm: 20x this)")
     ap.add_argument("--m-list", type=str, default=None,
                     help="comma-separated subset of the M sweep (for profiling one launch shape)")
     args = ap.parse_args()

@@ -251,8 +251,15 @@ bi_status bi_attention_ws(const bi_tensor* q, const bi_tensor* k, const bi_tenso
  * BI_ERR_INVALID_ARG before any launch (use bi_attention_ws).  The scratch is
  * shared by every call on the device, so calls must not overlap: issue them
  * on one stream or order them.  Results are those of bi_attention_ws, bit
- * for bit.  The pages have no counterpart of this entry point: it packages
- * the same operation for callers that cannot allocate device memory.
+ * for bit.  The scratch's device address is looked up (cudaGetSymbolAddress)
+ * on the first call on each device and again whenever that device's CUDA
+ * context has been replaced (after cudaDeviceReset); that first call should
+ * come before any stream capture.  No call allocates or frees device memory.
+ * The pages have no counterpart of this entry point: it packages the same
+ * operation for callers that cannot allocate device memory -- a serving
+ * engine whose allocator reserves all device memory up front and gives no
+ * library a way around it, or code that may not call cudaMalloc / cudaFree
+ * because those synchronise the device.
  */
 bi_status bi_attention_noalloc(const bi_tensor* q, const bi_tensor* k, const bi_tensor* v, float scale,
                                const bi_tensor* o, bi_stream stream);
@@ -262,13 +269,22 @@ bi_status bi_attention_noalloc(const bi_tensor* q, const bi_tensor* k, const bi_
  * and mean operations that "Unmasking the True Culprit: Why Temperature=0
  * Doesn't Mean Deterministic LLM Inference" (section "Beyond Matrix
  * Multiplication: Other Critical Operations") and "Batch-Invariant VLAs"
- * (aten::mean.dim) say must reduce each row in one fixed order.  Every row
- * is reduced by one warp in the order of bi_softmax_lastdim (4-element
- * groups g, lane g mod 32 adding its elements in ascending index order in
- * fp32, then a fixed xor butterfly), so a row's result does not depend on
- * how many rows are reduced with it, on where the row sits in memory or on
- * the launch.  Each add, multiply, divide and square root is one separately
- * rounded fp32 operation; the output is rounded once to its type.
+ * (aten::mean.dim) say must reduce each row in one fixed order.  A row of N
+ * elements is reduced by a team of T threads, T chosen from N and the input
+ * type alone: the first of 32, 64, 256, 1024 with N <= 4*G*T, G = 16 for
+ * 16-bit inputs and 8 for fp32.  The row is cut into groups of 4 consecutive
+ * elements; thread t adds the elements of groups t, t+T, t+2T, ... in
+ * ascending index order in fp32, each warp combines its 32 partials by a
+ * fixed xor butterfly, and the warp partials are added in warp order.  Rows
+ * longer than 4096*G elements are split, by N alone, over a cluster of
+ * cl = ceil(N / (4096*G)) <= 8 CTAs of 1024 threads: CTA r reduces the r-th
+ * of cl equal contiguous slices of the row's groups as above, and the cl
+ * slice totals are added in rank order.  The order therefore depends on N,
+ * the input type and the element index only -- not on how many rows are
+ * reduced together, on where the row sits in memory (aligned rows are loaded
+ * 4 elements at a time, others one at a time, with the same arithmetic) or
+ * on the launch.  Each add, multiply, divide and square root is one
+ * separately rounded fp32 operation; the output is rounded once to its type.
  *
  * All three: x (or s): [R,N] bf16, fp16 or fp32 with a unit stride on N,
  * aligned to its element size, N <= 2^24; outputs of any of the three types.

@@ -30,8 +30,13 @@ thread_local std::string t_last_error;
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
+// What the library caches per device belongs to one CUDA context (the device
+// addresses of its __device__ variables, kernel attributes): it is dropped and
+// resolved again when the device's current context is another one, as after
+// cudaDeviceReset and the primary context's re-creation.
 struct DevState {
   bool ready = false;
+  unsigned long long ctx_id = 0;  // the context the entries below were resolved in
   bi_status status = BI_OK;
   std::string why;
   int num_sms = 0;
@@ -44,6 +49,32 @@ DevState g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+bool g_ctx_tried = false;
+
+// Unique id of the calling thread's current CUDA context; 0 when none is
+// current (or the driver cannot say).  Caller holds g_mu.
+unsigned long long current_context_id() {
+  if (!g_ctx_tried) {
+    g_ctx_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    cudaGetLastError();
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_current || !g_ctx_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      g_ctx_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 bi_status finish(bi_status st, const std::string& why) {
   t_last_error = (st == BI_OK) ? std::string() : why;
@@ -66,6 +97,16 @@ bi_status current_device_info(DeviceInfo* info, std::string* why) {
   }
   std::lock_guard<std::mutex> lk(g_mu);
   DevState& d = g_dev[dev];
+  unsigned long long ctx = current_context_id();
+  if (ctx == 0) {
+    // No context is current on this thread yet: the runtime binds the
+    // device's primary context on first use, which this lookup is.
+    void* addr = nullptr;
+    cudaGetSymbolAddress(&addr, g_bi_status_word);
+    cudaGetLastError();
+    ctx = current_context_id();
+  }
+  if (d.ready && ctx != 0 && ctx != d.ctx_id) d = DevState();
   if (!d.ready) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -85,6 +126,7 @@ bi_status current_device_info(DeviceInfo* info, std::string* why) {
         d.status = BI_OK;
         d.num_sms = sms;
         d.status_word = reinterpret_cast<unsigned int*>(addr);
+        d.ctx_id = current_context_id();
       }
     }
     d.ready = true;

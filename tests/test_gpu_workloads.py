@@ -43,6 +43,21 @@ def test_llm_addmm_sweep():
     assert bits_equal(binding.bi_addmm(bg, xg, wg), full)
 
 
+def test_llm_addmm_packed_weight_equals_plain_full_size():
+    # The benchmark times the plain [4096,14336] weight; its packed form
+    # (bi_pack_weight) must give the same bits at every M of the sweep,
+    # including the full M = 8192 launch.
+    M_max = max(inputs.LLM_ADDMM_M)
+    x, w, bias = inputs.llm_addmm(M_max)
+    xg, wg, bg = x.cuda(), w.cuda(), bias.cuda()
+    wp = binding.bi_pack_weight(wg)
+    for M in inputs.LLM_ADDMM_M:
+        plain = binding.bi_addmm(bg, xg[:M], wg)
+        packed = binding.bi_addmm_packed(bg, xg[:M], wp)
+        assert bits_equal(plain, packed), f"packed and plain weights differ at M={M}"
+        del plain, packed
+
+
 def test_square_mm_sweep():
     # A [M,8192] ~N(0,1), W [8192,8192] ~N(0,0.01), fp32 out
     M_max = max(inputs.SQUARE_MM_M)
