@@ -314,7 +314,8 @@ def bits_equal(x, y) -> bool:
 
 def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -> dict:
     """The other workloads, once each: ours vs cuBLAS / cuDNN, with row-0 flags.
-    `only` restricts it to one workload (square, conv, attention, tiny, fp16, rows)."""
+    `only` restricts it to one workload (square, conv, attention, tiny, fp16, rows), or to
+    the attention's head-dimension sweep alone (heads)."""
     import torch.nn.functional as F
     from invariant_gemm_bi_gb300 import binding, inputs
     out = {}
@@ -327,6 +328,8 @@ def extra_sweeps(flush_buf, stream, peaks, reps: int, only: str | None = None) -
         _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point_fn(peaks))
     if want("attention"):
         _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point_fn(peaks))
+    if want("attention") or only == "heads":
+        _attention_heads(out, binding, inputs, flush_buf, stream, reps, point_fn(peaks))
     if want("tiny"):
         _tiny(out, binding, inputs, flush_buf, stream, 20 * reps)  # >= 1000 launches per point at reps >= 50
     if want("fp16"):
@@ -498,6 +501,13 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
                    binding.bi_attention_ws(ql[:1], kl[:1], vl[:1], 1.0 / 16), ol[:1])}
     del ql, kl, vl, ol, oc, ws
     out["attention_long"] = long_pt
+    out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0),
+                        "fused_head0_bit_equal_all_B": all(bits_equal(of0[B], of0[1]) for B in of0),
+                        "sdpa_head0_bit_equal_all_B": all(bits_equal(sd0[B], sd0[1]) for B in sd0)}
+    del q, k, v
+
+
+def _attention_heads(out, binding, inputs, flush_buf, stream, reps, point):
     # head dimensions 64, 128, 256 at the workload's token count (B = 32: 256
     # heads x 816 queries and keys), scale D^-1/2, bf16 out (as SDPA's)
     dims = []
@@ -513,10 +523,6 @@ def _attention(out, binding, inputs, flush_buf, stream, peaks, reps, point):
         dims.append({"D": d, "heads": Ld, "T": 816, "fused": point(fd, bd, td), "sdpa_us": round(tsd * 1e6, 2)})
         del qd, kd, vd, od
     out["attention_head_dims"] = dims
-    out["attention"] = {"points": res, "head0_bit_equal_all_B": all(bits_equal(o0[B], o0[1]) for B in o0),
-                        "fused_head0_bit_equal_all_B": all(bits_equal(of0[B], of0[1]) for B in of0),
-                        "sdpa_head0_bit_equal_all_B": all(bits_equal(sd0[B], sd0[1]) for B in sd0)}
-    del q, k, v
 
 
 def _rows(out, binding, inputs, flush_buf, stream, peaks, reps):
@@ -789,7 +795,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the cuBLAS comparison and the end-to-end pass (for profiling)")
-    ap.add_argument("--only", choices=["square", "conv", "attention", "tiny", "fp16", "rows"], default=None,
+    ap.add_argument("--only", choices=["square", "conv", "attention", "heads", "tiny", "fp16", "rows"],
+                    default=None,
                     help="measure only this workload (no headline line; for profiling)")
     ap.add_argument("--weight", choices=["packed", "plain"], default="plain",
                     help="weight path of the timed step (the other one is measured alongside)")

@@ -25,6 +25,7 @@ struct AttnParams {
   float* ws_ml;       // and (m, l) [ns][L][Tq][2]
   int32_t ns;         // key-range splits (1: not split)
   int32_t L, Tq, Tk, q_tiles, num_tiles;
+  int32_t pair_units, units;  // two-tile kernel: units holding two query tiles, all units
   float score_log2;  // scale * log2(e), rounded once to fp32
   int32_t out_f32;
   unsigned int* status_word;

@@ -299,3 +299,24 @@ def test_attention_head_dims_split(d, out_dtype):
     assert bits_equal(binding.bi_attention_ws(qg[1:2], kg[1:2], vg[1:2], d ** -0.5, out_dtype=out_dtype), full[1:2])
     assert bits_equal(binding.bi_attention_ws(qg[:, 130:].contiguous(), kg, vg, d ** -0.5, out_dtype=out_dtype),
                       full[:, 130:])
+
+
+@pytest.mark.parametrize("d", SMALL_D)
+def test_attention_two_tile_kernel_equals_one_tile_kernel(d):
+    # Heads of 64 or 128 with two or more query tiles run two tiles per CTA
+    # (pairs of tiles, then the odd last tile of each head alone: 100 heads x
+    # 5 tiles = 300 units, more than one per SM); a 128-row chunk on its own
+    # runs the one-tile kernel.  Every row has the same bits in both, also
+    # when the running maximum rises by more than 2^8 between key blocks.
+    L, Tq, Tk = 100, 640, 700
+    q, k, v = _qkv(L, Tq, Tk, 75, d)
+    k[:, 300:310] *= 6.0  # scores rise sharply at the third key block
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    for out_dtype in (torch.float32, torch.bfloat16):
+        full = binding.bi_attention(qg, kg, vg, d ** -0.5, out_dtype=out_dtype)
+        for c in range(Tq // 128):
+            part = binding.bi_attention(qg[:, 128 * c:128 * (c + 1)].contiguous(), kg, vg, d ** -0.5,
+                                        out_dtype=out_dtype)
+            assert bits_equal(part, full[:, 128 * c:128 * (c + 1)]), (out_dtype, c)
+    ref, absum, smax = oracle.attention(q[98:100], k[98:100], v[98:100], d ** -0.5)
+    check_attention(full[98:100], ref, absum, smax, Tk, f"two-tile D={d}")
