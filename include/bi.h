@@ -127,6 +127,16 @@ bi_status bi_bmm(const bi_tensor* a, const bi_tensor* b, const bi_tensor* c, flo
  *   y: [B,Co,Ho,Wo] bf16 or fp32 contiguous, Ho = (H+2ph-dh(KH-1)-1)/sh+1.
  *   stride, padding, dilation: {h, w}.  Each sample is computed as its own
  *   implicit-im2col product (the patch gather happens in shared memory).
+ *   Non-overlapping patches -- stride = (KH, KW), padding 0, dilation 1, one
+ *   group, KW even and <= 16, W a multiple of 8 and <= 256, W/KW <= 128, x
+ *   16-byte and w 4-byte aligned -- run the patch kernel of
+ *   bi_conv2d_patch_packed straight from w (its filter stages are built from
+ *   w in shared memory; nothing is allocated) and give its bits: each
+ *   tensor-core K = 16 step is one kernel row (ci, kh), kw padded with exact
+ *   zeros.  Every other geometry sums k in steps of 16 of the unfold order.
+ *   Which of the two runs is a function of the geometry and of the two
+ *   pointers' alignment, never of B (a batch slice of an aligned x stays
+ *   aligned); the two groupings agree within rounding, not bit for bit.
  */
 bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, const bi_tensor* bias,
                           const bi_tensor* y, const int32_t stride[2], const int32_t padding[2],
@@ -169,8 +179,8 @@ bi_status bi_conv_pack_weight(const bi_tensor* w, void* dst, int64_t dst_bytes,
  * tensor-core K = 16 step is one kernel row (ci, kh) (its zero slots add
  * exact zeros; image pixels outside a position's own window are never read
  * into it).  Per output element this is a fixed order, the same for every
- * batch size, but a different grouping than bi_conv2d_patch's: the two entry
- * points agree within rounding, not bit for bit.
+ * batch size, and the same as bi_conv2d_patch's for the geometries that
+ * bi_conv2d_patch runs on the patch kernel (bit for bit).
  *   x: [B,C,H,W] bf16 contiguous, 16-byte aligned, W a multiple of 8 and
  *      <= 256;  y: [B,Co,H/KH,W/KW] bf16 or fp32 contiguous, W/KW <= 128;
  *   bias: [Co] bf16 or fp32, or NULL / ptr == NULL.  Image rows or columns

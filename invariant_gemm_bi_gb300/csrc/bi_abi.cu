@@ -585,6 +585,38 @@ extern "C" bi_status bi_conv2d_patch(const bi_tensor* x, const bi_tensor* w, con
   if (!aligned(x->ptr, 2) || !aligned(w->ptr, 2) || !aligned(y->ptr, y->dtype == BI_F32 ? 4 : 2))
     return fail(BI_ERR_UNSUPPORTED_LAYOUT, "pointers must be aligned to their element size");
   if (C == 0 || KH * KW == 0) return fail(BI_ERR_INVALID_ARG, "empty reduction (C == 0)");
+  // Non-overlapping patches (stride = kernel, no padding, unit dilation, one
+  // group) run the patch kernel straight from this filter when the image rows
+  // suit its copies; which kernel runs depends on the geometry and on the
+  // alignment of x and w only, never on the batch size (a batch slice of an
+  // aligned x is aligned: a sample spans whole 16-byte rows).
+  const bool patch = stride[0] == KH && stride[1] == KW && padding[0] == 0 && padding[1] == 0 &&
+                     dilation[0] == 1 && dilation[1] == 1 && groups == 1 &&
+                     patch_plain_filter_ok(KH, KW, w->ptr) && (W * 2) % 16 == 0 && W <= 256 && Wo <= 128 &&
+                     patch_stage_bytes(W, patch_tile_rows(Ho, Wo, W)) <= kPatchStageMax &&
+                     aligned(x->ptr, 16) && C * KH * 16 <= INT32_MAX;
+  if (patch) {
+    if (B * C > INT32_MAX) return fail(BI_ERR_INVALID_ARG, "problem too large");
+    PatchProblem pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.x = x->ptr;
+    pp.w = w->ptr;
+    pp.bias = bias_kind ? bias->ptr : nullptr;
+    pp.bias_kind = bias_kind;
+    pp.y = y->ptr;
+    pp.out_f32 = y->dtype == BI_F32;
+    pp.B = B;
+    pp.C = C;
+    pp.H = H;
+    pp.W = W;
+    pp.Co = Co;
+    pp.KH = KH;
+    pp.KW = KW;
+    pp.Ho = Ho;
+    pp.Wo = Wo;
+    st = launch_patch(pp, (cudaStream_t)stream, &why);
+    return finish(st, why);
+  }
   ConvProblem cp;
   memset(&cp, 0, sizeof(cp));
   cp.x = x->ptr;

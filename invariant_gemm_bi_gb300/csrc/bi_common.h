@@ -96,7 +96,9 @@ constexpr int kPatchStageMax = 32768;
 // Non-overlapping patch convolution with a packed filter (see bi_patch.cu).
 struct PatchParams {
   CUtensorMap tma_x;  // x as {W, KH, Ho, B*C}, box {W, 4, t_oh, 1}, no swizzle
-  CUtensorMap tma_w;  // packed filter [Co][Kp], box {64, BN, 1}, 128B swizzle
+  CUtensorMap tma_w;  // packed filter [Co][Kp], box {64, BN, 1}, 128B swizzle (packed filter only)
+  const uint32_t* w_plain;  // or the filter as given, [Co][C][KH][KW] bf16 (KW 14 or 16), as bf16 pairs
+  int32_t KH;
   const void* bias;   // [Co] or null
   void* y;            // [B][Co][Ho][Wo] contiguous
   int32_t C, W, KW, Wo, khq;    // khq: K blocks per input channel (KH rounded up to 4, / 4)

@@ -132,7 +132,8 @@ bi_status launch_conv(const ConvProblem& cp, cudaStream_t stream, std::string* w
 // Non-overlapping patch convolution with a packed filter (bi_patch.cu).
 struct PatchProblem {
   const void* x;   // [B][C][H][W] bf16 contiguous, 16-byte aligned, W*2 % 16 == 0
-  const void* wp;  // packed filter [Co][patch_padded_k(C, KH)]
+  const void* wp;  // packed filter [Co][patch_padded_k(C, KH)], or null:
+  const void* w;   // the filter as given, [Co][C][KH][KW] bf16 contiguous (patch_plain_filter_ok)
   const void* bias;
   int bias_kind;
   void* y;  // [B][Co][Ho][Wo] contiguous
@@ -141,6 +142,9 @@ struct PatchProblem {
 };
 // Row length of the packed filter: C * (KH rounded up to 4) * 16.
 int64_t patch_padded_k(int64_t C, int64_t KH);
+// Whether the patch kernel can build its filter stages from the filter as
+// given: KW = 16, or KW = 14 with KH even; w 16-byte aligned.
+bool patch_plain_filter_ok(int64_t KH, int64_t KW, const void* w);
 // Shared memory of one staged K block of image rows (t_oh output rows of an
 // image W pixels wide); at most kPatchStageMax.
 int64_t patch_stage_bytes(int64_t W, int64_t t_oh);

@@ -25,7 +25,9 @@
 // 192 channels): it never mixes samples, so one sample's arithmetic is the
 // same for every batch size.
 //
-//   warp 0      filter producer (TMA, a ring of 4 stages)
+//   warp 0      filter producer (TMA, a ring of 4 stages); with the filter
+//               as given (not packed), warps 0 and 11-13 build each filter
+//               stage instead (below)
 //   warp 1      TMEM allocator + UMMA issuer (128 x 192 x 16, cta_group::1,
 //               A from TMEM, B = the filter block from shared memory)
 //   warps 2..5  epilogue: tcgen05.ld -> + bias -> rounding -> y (NCHW: the
@@ -78,7 +80,119 @@ struct StgRing {
 };
 
 constexpr int kPatchThreads = 352;
-constexpr int kPatchBuilders = 128;  // warps 6..9
+constexpr int kPatchThreadsPlain = 448;  // + warps 11..13: filter builders with warp 0
+constexpr int kPatchBuilders = 128;      // warps 6..9
+constexpr int kPatchFilterBuilders = 128;
+
+// Filter builders (the filter as given, KW = 14 or 16): a K block's [192
+// channels x 64 k] filter block laid out exactly as the TMA copy of the
+// packed filter lays it out -- row r (channel nb*192 + r) of 128 bytes, its
+// 16-byte unit u at u ^ (r % 8) (the 128-byte swizzle), words 8g .. 8g + 7 of
+// the row holding kw = 0 .. 15 of kernel row kh0 + g as bf16 pairs -- with
+// zeros for kw >= KW, kh >= KH and channels past Co.  A channel's kernel rows
+// kh0 .. kh0 + 3 are one contiguous run of the filter (4 KW bf16), so thread
+// t (0..127) reads half rows t, t + 128 and t + 256 (two kernel rows of a
+// channel each) with 8-byte (KW = 14) or 16-byte (KW = 16) loads and writes
+// each with four 16-byte stores, the pad words in place.  The pieces of the
+// next two K blocks are in flight while a stage is waited for and written.
+template <int KW>
+struct FilterRun {
+  static constexpr int kWords = KW;  // 2 kernel rows of KW bf16, as 32-bit words
+  uint32_t w[3][kWords];             // half rows t, t + 128, t + 256
+};
+
+// Half row hr = 2 r + h2 of the block: kernel rows kh0 + 2 h2, kh0 + 2 h2 + 1
+// of channel nb*192 + r.
+template <int KW>
+__device__ __forceinline__ void filter_load(const PatchParams& p, int t, int nb, int kb, FilterRun<KW>& f) {
+  const int ci = kb / p.khq;
+  const int kh0 = (kb - ci * p.khq) * 4;
+  const int rows = min(4, p.KH - kh0);  // kernel rows of this block inside the filter
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int hr = t + 128 * j, r = hr >> 1, h2 = hr & 1;
+    const int co = nb * kPatchBN + r;
+    const bool live = co < p.Co && 2 * h2 < rows;  // KW = 14: rows is even, a half row is whole or absent
+    const uint32_t* src = p.w_plain + (((int64_t)co * p.C + ci) * p.KH + kh0 + 2 * h2) * (KW / 2);
+    if (KW == 16) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 16-byte pieces, two per kernel row
+        const bool in = co < p.Co && 2 * h2 + c / 2 < rows;
+        const uint4 v = in ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
+        f.w[j][4 * c] = v.x;
+        f.w[j][(4 * c + 1) % KW] = v.y;
+        f.w[j][(4 * c + 2) % KW] = v.z;
+        f.w[j][(4 * c + 3) % KW] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < KW / 2; ++c) {  // 8-byte pieces
+        const uint2 v = live ? __ldg(reinterpret_cast<const uint2*>(src) + c) : make_uint2(0u, 0u);
+        f.w[j][2 * c] = v.x;
+        f.w[j][2 * c + 1] = v.y;
+      }
+    }
+  }
+}
+
+template <int KW>
+__device__ __forceinline__ void filter_store(uint32_t dst, int t, const FilterRun<KW>& f) {
+  constexpr int kw2 = KW / 2;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int hr = t + 128 * j, r = hr >> 1, h2 = hr & 1;
+    const uint32_t row = dst + r * 128;
+#pragma unroll
+    for (int uu = 0; uu < 4; ++uu) {  // unit u = 4 h2 + uu: kernel row 2 h2 + uu / 2, pairs 4 (uu % 2) ..
+      uint32_t q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int g = uu / 2, e = 4 * (uu % 2) + i;
+        q[i] = e < kw2 ? f.w[j][g * kw2 + e] : 0u;
+      }
+      const int u = 4 * h2 + uu;
+      st_shared_v4(row + ((uint32_t)(u ^ (r & 7)) << 4), q[0], q[1], q[2], q[3]);
+    }
+  }
+}
+
+template <int KW>
+__device__ __forceinline__ void patch_filter_builder(const PatchParams& p, uint32_t sB, const PipeBars& bars, int t,
+                                                     const WaitCtl& wc) {
+  using Lay = PatchLayout;
+  const int lane = t & 31;
+  FilterRun<KW> f0, f1;
+  int tile_ld = blockIdx.x, kb_ld = 0;  // the next block to load
+  auto load_next = [&](FilterRun<KW>& dst) {
+    if (tile_ld >= p.num_tiles) return;
+    filter_load<KW>(p, t, decode_tile(tile_ld, p.m_tiles, p.n_tiles).nb, kb_ld, dst);
+    if (++kb_ld == p.k_blocks) {
+      kb_ld = 0;
+      tile_ld += gridDim.x;
+    }
+  };
+  load_next(f0);
+  load_next(f1);
+  const uint32_t total = (uint32_t)max(0, (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) *
+                         (uint32_t)p.k_blocks;
+  // Block it from cur, then cur takes block it + 2.
+  auto step = [&](uint32_t it, FilterRun<KW>& cur) -> bool {
+    const uint32_t s = it % Lay::STAGES, r = it / Lay::STAGES;
+    const bool got = r == 0 || mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
+                                                  wc.limit_ns, status_code(6, kSiteProducerEmpty));
+    if (!__all_sync(0xffffffffu, got)) return false;
+    filter_store<KW>(sB + s * Lay::B_BYTES, t, cur);
+    fence_proxy_async_smem();  // the tensor core reads the stage through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.full(s));
+    load_next(cur);
+    return true;
+  };
+  for (uint32_t it = 0; it < total; it += 2) {
+    if (!step(it, f0)) break;
+    if (it + 1 < total && !step(it + 1, f1)) break;
+  }
+}
 
 // Patch-tile row r (one output position; zeros past the tile's positions) of
 // one K block from the staged image rows, as the 32 TMEM columns of the
@@ -157,7 +271,9 @@ __device__ __forceinline__ void patch_mma(uint32_t sB, const PipeBars& bars, uin
   mbar_wait_bounded(bars.drain, 0, nullptr, w.status_word, w.limit_ns, status_code(6, kSiteDrain));
 }
 
-__global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_constant__ PatchParams p) {
+template <bool PLAIN>
+__global__ void __launch_bounds__(PLAIN ? kPatchThreadsPlain : kPatchThreads, 1)
+    patch_kernel(const __grid_constant__ PatchParams p) {
   using Lay = PatchLayout;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -182,10 +298,11 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    // A stage is full when its filter block has landed and the four builder
-    // warps have written its patch tile into TMEM.
+    // A stage is full when its filter block has landed (or the four filter
+    // builder warps have written it) and the four patch builder warps have
+    // written its patch tile into TMEM.
     for (int s = 0; s < Lay::STAGES; ++s) {
-      mbar_init(bars.full(s), 1 + kPatchBuilders / 32);
+      mbar_init(bars.full(s), (PLAIN ? kPatchFilterBuilders / 32 : 1) + kPatchBuilders / 32);
       mbar_init(bars.empty(s), 1);
     }
     for (int q = 0; q < ring.n; ++q) {
@@ -200,7 +317,7 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&p.tma_x);
-    tma_prefetch_desc(&p.tma_w);
+    if (!PLAIN) tma_prefetch_desc(&p.tma_w);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
@@ -212,7 +329,13 @@ __global__ void __launch_bounds__(kPatchThreads, 1) patch_kernel(const __grid_co
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status_word, p.wait_limit_ns};
 
-  if (warp == 0) {
+  if (PLAIN && (warp == 0 || warp >= 11)) {
+    const int t = (warp == 0 ? 0 : warp - 10) * 32 + lane;
+    if (p.KW == 16)
+      patch_filter_builder<16>(p, sB, bars, t, wc);
+    else
+      patch_filter_builder<14>(p, sB, bars, t, wc);
+  } else if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -354,6 +477,13 @@ __global__ void conv_pack_kernel(const uint16_t* __restrict__ w, uint16_t* __res
 
 int64_t patch_padded_k(int64_t C, int64_t KH) { return C * ((KH + 3) / 4 * 4) * 16; }
 
+// The filter builders read a channel's kernel-row runs with 16-byte (KW = 16)
+// or 8-byte (KW = 14: a run starts at ((co C + ci) KH + kh0) 28 bytes, a
+// multiple of 8 when KH is even) loads.
+bool patch_plain_filter_ok(int64_t KH, int64_t KW, const void* w) {
+  return (KW == 16 || (KW == 14 && KH % 2 == 0)) && reinterpret_cast<uintptr_t>(w) % 16 == 0;
+}
+
 int64_t patch_stage_bytes(int64_t W, int64_t t_oh) { return W * 4 * t_oh * 2; }
 
 int64_t patch_tile_rows(int64_t Ho, int64_t Wo, int64_t W) {
@@ -400,7 +530,14 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
                       const_cast<void*>(pp.x), 4, dims, strides, box, why))
       return BI_ERR_CUDA;
   }
-  {
+  const bool plain = pp.wp == nullptr;
+  if (plain) {
+    if (!patch_plain_filter_ok(pp.KH, pp.KW, pp.w)) {
+      *why = "the filter as given needs KW = 14 (with KH even) or 16, 16-byte aligned";
+      return BI_ERR_UNSUPPORTED_LAYOUT;
+    }
+    p.w_plain = static_cast<const uint32_t*>(pp.w);
+  } else {
     const cuuint64_t dims[3] = {(cuuint64_t)Kp, (cuuint64_t)pp.Co, 1};
     const cuuint64_t strides[2] = {(cuuint64_t)Kp * 2, (cuuint64_t)(Kp * 2 * pp.Co)};
     const cuuint32_t box[3] = {kBK, kPatchBN, 1};
@@ -412,6 +549,7 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
   p.C = (int32_t)pp.C;
   p.W = (int32_t)pp.W;
   p.KW = (int32_t)pp.KW;
+  p.KH = (int32_t)pp.KH;
   p.Wo = (int32_t)pp.Wo;
   p.khq = (int32_t)((pp.KH + 3) / 4);
   p.t_oh = (int32_t)t_oh;
@@ -432,10 +570,15 @@ bi_status launch_patch(const PatchProblem& pp, cudaStream_t stream, std::string*
   p.bias_kind = pp.bias_kind;
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&patch_kernel), PatchLayout::DYN_BYTES, 6);
+  const void* fn = plain ? reinterpret_cast<const void*>(&patch_kernel<true>)
+                         : reinterpret_cast<const void*>(&patch_kernel<false>);
+  cudaError_t e = set_smem_once(fn, PatchLayout::DYN_BYTES, plain ? 15 : 6);
   if (e == cudaSuccess) {
     const int grid = (int)std::min<int64_t>(tiles, dev.num_sms);
-    patch_kernel<<<grid, kPatchThreads, PatchLayout::DYN_BYTES, stream>>>(p);
+    if (plain)
+      patch_kernel<true><<<grid, kPatchThreadsPlain, PatchLayout::DYN_BYTES, stream>>>(p);
+    else
+      patch_kernel<false><<<grid, kPatchThreads, PatchLayout::DYN_BYTES, stream>>>(p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -116,3 +116,37 @@ def test_distractor_samples_do_not_touch_sample0():
         d[1:] = fill
         y = binding.bi_conv2d_patch_packed(d.cuda(), packed, bias.cuda())
         assert bits_equal(y[:1], alone)
+
+
+@pytest.mark.parametrize("case", [c for c in PATCH_CASES if c[6] == 16 or (c[6] == 14 and c[5] % 2 == 0)] +
+                         [(32, 3, 224, 224, 1152, 14, 14, torch.bfloat16, torch.bfloat16),
+                          (2, 3, 45, 64, 200, 9, 16, torch.float32, None)])  # KH = 9: a lone kernel row per channel
+def test_plain_filter_entry_point_equals_packed(case):
+    # bi_conv2d_patch on non-overlapping 16-wide patches, or 14-wide ones with
+    # an even patch height, builds the packed filter layout in shared memory
+    # from w itself: the bits of the packed path.
+    B, C, H, W, Co, KH, KW, od, bd = case
+    x = inputs.uniform_bf16((B, C, H, W), -1, 1, 46)
+    w = inputs.normal_bf16((Co, C, KH, KW), 0.05, 47)
+    bias = None if bd is None else inputs.normal_bf16((Co,), 0.1, 48).to(bd).cuda()
+    xg, wg = x.cuda(), w.cuda()
+    packed = binding.bi_conv2d_patch_packed(xg, binding.bi_conv_pack_weight(wg), bias, out_dtype=od)
+    plain = binding.bi_conv2d_patch(xg, wg, bias, stride=(KH, KW), out_dtype=od)
+    assert bits_equal(plain, packed)
+    for b in (1, B):
+        assert bits_equal(binding.bi_conv2d_patch(xg[:b], wg, bias, stride=(KH, KW), out_dtype=od), packed[:b])
+
+
+def test_plain_filter_entry_point_misaligned_image_takes_the_general_kernel():
+    # An image view that is not 16-byte aligned cannot be copied by rows: the
+    # general kernel runs (the unfold order in steps of 16), within the
+    # oracle's bound.
+    B, C, H, W, Co, KH, KW = 2, 3, 32, 48, 40, 8, 8
+    x = inputs.uniform_bf16((B, C, H, W), -1, 1, 49)
+    w = inputs.normal_bf16((Co, C, KH, KW), 0.1, 50)
+    buf = torch.zeros(x.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    xs = buf[1:].view(B, C, H, W)
+    xs.copy_(x.cuda())
+    y = binding.bi_conv2d_patch(xs, w.cuda(), None, stride=(KH, KW), out_dtype=torch.float32)
+    ref, absum = oracle.conv2d(x, w, None, (KH, KW), 0, 1, 1)
+    check_tolerance(y, ref, absum, "misaligned image")
