@@ -407,7 +407,8 @@ def _fp16(out, binding, inputs, flush_buf, stream, peaks, reps, point):
 
 def _conv(out, binding, inputs, F, flush_buf, stream, peaks, reps, point):
     # packed filter (bi_conv2d_patch_packed, packed once like the linear weight),
-    # the plain-filter general kernel (bi_conv2d_patch) and cuDNN on the same shapes
+    # the filter as given (bi_conv2d_patch: the same patch kernel, its filter
+    # stages built from w) and cuDNN on the same shapes
     x, wc, bc = inputs.patch_embed(max(inputs.PATCH_EMBED_B), device="cuda")
     wpk = binding.bi_conv_pack_weight(wc)
     res, y0, yp0, yc0 = [], {}, {}, {}
