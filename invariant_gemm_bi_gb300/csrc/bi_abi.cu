@@ -41,8 +41,8 @@ struct DevState {
   std::string why;
   int num_sms = 0;
   unsigned int* status_word = nullptr;
-  bool smem_set[16] = {};
-  int pairs[16] = {};  // resident 2-CTA clusters per kernel slot (0: not yet asked)
+  bool smem_set[24] = {};
+  int pairs[24] = {};  // resident 2-CTA clusters per kernel slot (0: not yet asked)
   void* scratch = nullptr;  // device address of g_bi_noalloc_scratch (0: not yet asked)
 };
 DevState g_dev[kMaxDevices];

@@ -1126,7 +1126,7 @@ bool attention_head_dim_ok(int64_t D) { return D == 64 || D == 128 || D == 256; 
 template <int D>
 static cudaError_t attn_launch_d(const AttnParams& p, int64_t tiles, int num_sms, cudaStream_t stream) {
   using C = AttnCfg<D>;
-  const int slot = D == 256 ? 7 : D == 128 ? 12 : 13;  // the GEMMs hold 0-3 and 8-11
+  const int slot = D == 256 ? 7 : D == 128 ? 12 : 13;  // the GEMMs hold 0-3, 8-11 and 16-19
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&attn_kernel<D>), C::DYN, slot);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<int64_t>(tiles, num_sms);

@@ -96,7 +96,7 @@ __device__ __forceinline__ TileCoord pair_tile(int tile, const GemmParams& p, ui
 // M) and its half of the tile's B columns, into its own shared memory.  Every
 // copy of both CTAs completes on the even CTA's full barrier of the stage,
 // which the even CTA arms with the bytes of both.
-template <bool B_MN, bool B_PACKED, int A_ROWS>
+template <bool B_MN, bool B_PACKED, int A_ROWS, bool STREAM_B>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, uint32_t sB,
                                             const PipeBars& bars, const ProdCursor& c,
                                             uint32_t crank) {
@@ -111,19 +111,30 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sA, ui
   const uint32_t fb = cluster_map_shared(bars.full(s), 0);
   const uint32_t b_dst = sB + s * Lay::B_BYTES;
   const int n0 = tc.nb * kGemmBN + (int)crank * (kGemmBN / 2);
+  // STREAM_B (at most two 256-row tiles): each block of B is used by one or
+  // two CTA pairs and never again, so it is loaded with the evict-first L2
+  // priority and the A rows, which every column tile reads again, with
+  // evict-last.  Otherwise both take the default priority.  Data movement
+  // only: the arithmetic is the same either way.
+  auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2, bool is_b) {
+    if (STREAM_B)
+      tma_load_3d_pair_hint(dst, map, fb, c0, c1, c2,
+                            is_b ? l2_policy_evict_first() : l2_policy_evict_last());
+    else
+      tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+  };
   if (B_PACKED) {
     // The packed weight as rows of 128 bytes: this CTA's columns n0 .. are
     // whole 64-column chunks, B_BYTES / 128 consecutive rows of the image.
     const int64_t byte0 = (int64_t)c.kb * p.packed_kb_stride + (int64_t)(n0 / kPackChunk) * kPackChunkBytes;
-    tma_load_3d_pair(b_dst, &p.tma_b, fb, 0, (int32_t)(byte0 / 128), 0);
+    load(b_dst, &p.tma_b, 0, (int32_t)(byte0 / 128), 0, true);
   } else if (B_MN) {
 #pragma unroll
-    for (int j = 0; j < kGemmBN / 2 / 64; ++j)
-      tma_load_3d_pair(b_dst + j * 8192, &p.tma_b, fb, n0 + j * 64, c.kb * kBK, tc.l);
+    for (int j = 0; j < kGemmBN / 2 / 64; ++j) load(b_dst + j * 8192, &p.tma_b, n0 + j * 64, c.kb * kBK, tc.l, true);
   } else {
-    tma_load_3d_pair(b_dst, &p.tma_b, fb, c.kb * kBK, n0, tc.l);
+    load(b_dst, &p.tma_b, c.kb * kBK, n0, tc.l, true);
   }
-  if (a_live) tma_load_3d_pair(sA + s * Lay::A_BYTES, &p.tma_a, fb, c.kb * kBK, tc.mb * kBM, tc.l);
+  if (a_live) load(sA + s * Lay::A_BYTES, &p.tma_a, c.kb * kBK, tc.mb * kBM, tc.l, false);
 }
 
 __device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int stride,
@@ -136,7 +147,7 @@ __device__ __forceinline__ void advance(ProdCursor& c, const GemmParams& p, int 
   }
 }
 
-template <bool B_MN, bool B_PACKED, int A_ROWS>
+template <bool B_MN, bool B_PACKED, int A_ROWS, bool STREAM_B>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
   using Lay = GemmLayout<A_ROWS>;
@@ -196,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   cluster_arrive_relaxed();
   if (threadIdx.x == 0) {
     while (crank == 0 && cur.it < (uint32_t)Lay::STAGES && cur.tile < p.num_tiles) {
-      issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur, crank);
+      issue_stage<B_MN, B_PACKED, A_ROWS, STREAM_B>(p, sA, sB, bars, cur, crank);
       advance(cur, p, stride, crank);
     }
   }
@@ -212,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (r > 0 && !mbar_wait_bounded(bars.empty(s), (r - 1) & 1, wc.abort, wc.status_word,
                                         wc.limit_ns, status_code(6, kSiteProducerEmpty)))
           break;
-        issue_stage<B_MN, B_PACKED, A_ROWS>(p, sA, sB, bars, cur, crank);
+        issue_stage<B_MN, B_PACKED, A_ROWS, STREAM_B>(p, sA, sB, bars, cur, crank);
         advance(cur, p, stride, crank);
       }
       // No copy may still be landing in shared memory, and no MMA-completion
@@ -368,28 +379,28 @@ bi_status launch_pack(const GemmProblem& g, void* dst, cudaStream_t stream, std:
 }
 
 // Grid: two CTAs per pair, min(#tiles, #pairs that fit at once) pairs.
-template <bool B_MN, bool B_PACKED, int A_ROWS>
+template <bool B_MN, bool B_PACKED, int A_ROWS, bool STREAM_B>
 static cudaError_t launch_variant(const GemmParams& p, int64_t tiles, cudaStream_t stream, int slot) {
   using Lay = GemmLayout<A_ROWS>;
-  const void* fn = reinterpret_cast<const void*>(&gemm_kernel<B_MN, B_PACKED, A_ROWS>);
+  const void* fn = reinterpret_cast<const void*>(&gemm_kernel<B_MN, B_PACKED, A_ROWS, STREAM_B>);
   cudaError_t e = set_smem_once(fn, Lay::DYN_BYTES, slot);
   if (e != cudaSuccess) return e;
   int pairs = 0;
   e = pair_capacity(fn, kGemmThreads, Lay::DYN_BYTES, slot, &pairs);
   if (e != cudaSuccess) return e;
   const int grid = 2 * (int)std::min<int64_t>(tiles, pairs);
-  gemm_kernel<B_MN, B_PACKED, A_ROWS><<<grid, kGemmThreads, Lay::DYN_BYTES, stream>>>(p);
+  gemm_kernel<B_MN, B_PACKED, A_ROWS, STREAM_B><<<grid, kGemmThreads, Lay::DYN_BYTES, stream>>>(p);
   return cudaSuccess;
 }
 
-template <int A_ROWS>
+template <int A_ROWS, bool STREAM_B>
 static cudaError_t launch_rows(const GemmProblem& g, const GemmParams& p, int64_t tiles,
                                cudaStream_t stream, int slot0) {
   if (g.b_packed)
-    return g.b_mn_major ? launch_variant<true, true, A_ROWS>(p, tiles, stream, slot0 + 2)
-                        : launch_variant<false, true, A_ROWS>(p, tiles, stream, slot0 + 3);
-  return g.b_mn_major ? launch_variant<true, false, A_ROWS>(p, tiles, stream, slot0)
-                      : launch_variant<false, false, A_ROWS>(p, tiles, stream, slot0 + 1);
+    return g.b_mn_major ? launch_variant<true, true, A_ROWS, STREAM_B>(p, tiles, stream, slot0 + 2)
+                        : launch_variant<false, true, A_ROWS, STREAM_B>(p, tiles, stream, slot0 + 3);
+  return g.b_mn_major ? launch_variant<true, false, A_ROWS, STREAM_B>(p, tiles, stream, slot0)
+                      : launch_variant<false, false, A_ROWS, STREAM_B>(p, tiles, stream, slot0 + 1);
 }
 
 bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* why) {
@@ -454,8 +465,11 @@ bi_status launch_gemm(const GemmProblem& g, cudaStream_t stream, std::string* wh
   p.status_word = dev.status_word;
   p.wait_limit_ns = kWaitLimitNs;
 
-  cudaError_t e = short_a ? launch_rows<kShortARows>(g, p, tiles, stream, 8)
-                          : launch_rows<kBM>(g, p, tiles, stream, 0);
+  // Kernel slots: 0-3 general layout, 16-19 the same with the weight
+  // streamed (at most two row tiles), 8-11 short A (always one row tile).
+  cudaError_t e = short_a         ? launch_rows<kShortARows, true>(g, p, tiles, stream, 8)
+                  : p.m_tiles <= 2 ? launch_rows<kBM, true>(g, p, tiles, stream, 16)
+                                   : launch_rows<kBM, false>(g, p, tiles, stream, 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("gemm launch: ") + cudaGetErrorString(e);
