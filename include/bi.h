@@ -315,7 +315,10 @@ bi_status bi_rmsnorm_lastdim(const bi_tensor* x, const bi_tensor* weight, float 
 /*
  * y[r,j] = RN(RN(s[r,j] - mx) - lse),  mx = max_j s[r,j],
  *   lse = logf(sum_j expf(RN(s[r,j] - mx))).
- * y: [R,N], unit stride on N.
+ * y: [R,N], unit stride on N.  For 1024-thread teams, when the rows' clusters
+ * are more than the GPU runs at once with each thread holding its groups in
+ * registers, each pass reloads them instead (two CTAs per SM); the order
+ * above, and so every bit, is the same either way.
  */
 bi_status bi_log_softmax_lastdim(const bi_tensor* s, const bi_tensor* y, bi_stream stream);
 

@@ -66,6 +66,14 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // A float at the shared::cluster address `addr` (from cluster_map_shared).
+// Asks L2 to fetch the `bytes` bytes at global address p (16-byte aligned, a
+// multiple of 16 bytes, inside one allocation); no register receives data.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)__cvta_generic_to_global(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

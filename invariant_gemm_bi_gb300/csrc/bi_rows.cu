@@ -87,7 +87,12 @@ bi_status launch_row_reduction(int op, const RowParams& rp_in, cudaStream_t stre
   if (op == kRowRmsNorm) {
     launch_rmsnorm_rows(T, rp, grid, stream);
   } else if (op == kRowLogSoftmax) {
-    launch_log_softmax_rows(T, rp, grid, stream);
+    // 1024-thread teams hold a chunk in registers, one CTA per SM (and a
+    // cluster's CTAs within one GPC): when the rows' clusters need more than
+    // one wave of that kernel, the streaming form (two CTAs per SM, the same
+    // bits) runs them instead.
+    const bool stream_form = T == 1024 && (int64_t)grid.x > log_softmax_register_capacity(rp);
+    launch_log_softmax_rows(T, rp, grid, stream_form, stream);
   } else {
     switch (T) {
       case 32: launch_mean_t<32>(rp, grid, stream); break;

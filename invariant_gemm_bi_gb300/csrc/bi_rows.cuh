@@ -158,10 +158,11 @@ __device__ __forceinline__ RowSpan row_span(int N, int cl, int rank) {
 // k = 0..G-1, g0 = gbeg + GcT + t, as raw words (zeros past the end of the
 // span).  All loads are issued before any value is used.  `full`: all G
 // groups lie inside the span and the row and were loaded as vectors (no
-// per-element checks needed).
-template <int X>
+// per-element checks needed).  A piece (GN < G) holds GN consecutive groups
+// k0 .. k0 + GN - 1 of a chunk, with g0 its first.
+template <int X, int GN = chunk_groups<X>()>
 struct RowChunk {
-  static constexpr int G = chunk_groups<X>();
+  static constexpr int G = GN;
   uint32_t w[G][Elem<X>::kWords];
   int g0, gend;
   bool full;
@@ -173,12 +174,12 @@ __device__ __forceinline__ int group_n(int g, int gend, int N) {
   return g >= gend ? 0 : (g < nfull ? 4 : (g == nfull ? (N & 3) : 0));
 }
 
-template <int T, int X>
+template <int T, int X, int GN>
 __device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, const RowSpan& sp, int t, int c,
-                                           RowChunk<X>& ch) {
+                                           RowChunk<X, GN>& ch, int k0 = 0) {
   constexpr int W = Elem<X>::kWords;
-  constexpr int G = RowChunk<X>::G;
-  ch.g0 = sp.gbeg + c * G * T + t;
+  constexpr int G = GN;
+  ch.g0 = sp.gbeg + (c * chunk_groups<X>() + k0) * T + t;
   ch.gend = sp.gend;
   ch.full = vec && ch.g0 + (G - 1) * T < min(N >> 2, sp.gend);
   if (ch.full) {
@@ -222,22 +223,22 @@ __device__ __forceinline__ void load_chunk(const void* x, bool vec, int N, const
 }
 
 // Elements of group k of the chunk that lie inside the span (0 past its end).
-template <int T, int X>
-__device__ __forceinline__ int chunk_n(const RowChunk<X>& ch, int k, int N) {
+template <int T, int X, int GN>
+__device__ __forceinline__ int chunk_n(const RowChunk<X, GN>& ch, int k, int N) {
   return ch.full ? 4 : group_n(ch.g0 + k * T, ch.gend, N);
 }
 
 // f(value) over the chunk's elements, groups then elements ascending.
-template <int T, int X, typename F>
-__device__ __forceinline__ void chunk_visit(const RowChunk<X>& ch, int N, F&& f) {
+template <int T, int X, int GN, typename F>
+__device__ __forceinline__ void chunk_visit(const RowChunk<X, GN>& ch, int N, F&& f) {
   if (ch.full) {
 #pragma unroll
-    for (int k = 0; k < RowChunk<X>::G; ++k)
+    for (int k = 0; k < GN; ++k)
 #pragma unroll
       for (int i = 0; i < 4; ++i) f(word_val<X>(ch.w[k], i));
   } else {
 #pragma unroll
-    for (int k = 0; k < RowChunk<X>::G; ++k) {
+    for (int k = 0; k < GN; ++k) {
       const int n = chunk_n<T, X>(ch, k, N);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -388,6 +389,12 @@ int row_cluster_size(int64_t N, int x_kind);
 // Launchers of the three operations for team size T (bi_rows_rms.cu,
 // bi_rows_lsm.cu, bi_rows.cu); grid: one block per Team<T>::kRows rows.
 void launch_rmsnorm_rows(int T, const RowParams& rp, dim3 grid, cudaStream_t stream);
-void launch_log_softmax_rows(int T, const RowParams& rp, dim3 grid, cudaStream_t stream);
+// CTAs of the register-resident 1024-thread log-softmax kernel (for rp's
+// types and cluster size) that run at once on the current device; 0 if the
+// occupancy query fails.
+int log_softmax_register_capacity(const RowParams& rp);
+// stream_form: the log-softmax's streaming form (1024-thread teams only; the
+// same bits as the register-resident form).
+void launch_log_softmax_rows(int T, const RowParams& rp, dim3 grid, bool stream_form, cudaStream_t stream);
 
 }  // namespace bi

@@ -185,6 +185,34 @@ def test_misaligned_and_strided_rows_give_the_same_bits(N):
     assert bool((mbig[1::2] == 7.0).all())
 
 
+# Long rows reduced by clusters of 1024-thread CTAs: when the rows' clusters
+# take more than one wave of SMs the kernel streams each thread's groups from
+# memory on every pass instead of holding them in registers.  The row count
+# picks the form; the bits must not depend on it.
+LONG_ROWS = [(torch.float32, 128256, 40), (torch.float32, 40003, 90), (torch.bfloat16, 70001, 80),
+             (torch.float16, 600001, 20), (torch.bfloat16, 40003, 160)]
+
+
+@pytest.mark.parametrize("x_dtype,N,R", LONG_ROWS)
+def test_log_softmax_streaming_form_equals_register_form(x_dtype, N, R):
+    s = _x((R, N), x_dtype, 3.0, 11)
+    s[3, ::5] = float("-inf")  # a masked row
+    sg = s.cuda()
+    for yd in (torch.float32, x_dtype):
+        full = binding.bi_log_softmax_lastdim(sg, out_dtype=yd)  # more clusters than SMs
+        for r in (0, 3, R // 2, R - 1):
+            assert bits_equal(binding.bi_log_softmax_lastdim(sg[r:r + 1], out_dtype=yd), full[r:r + 1]), (yd, r)
+        assert bits_equal(binding.bi_log_softmax_lastdim(sg[:7], out_dtype=yd), full[:7]), yd
+        rows = [0, 3, R - 1]
+        check_log_softmax(full[rows], oracle.log_softmax_rows(s[rows]), N, f"streamed {x_dtype} {N} -> {yd}")
+    # rows off a 4-element boundary (element loads) give the same bits
+    store = torch.zeros((R, N + 3), dtype=x_dtype)
+    store[:, 1:N + 1] = s
+    xs = store.cuda()[:, 1:N + 1]
+    assert bits_equal(binding.bi_log_softmax_lastdim(xs), binding.bi_log_softmax_lastdim(sg))
+    assert bits_equal(binding.bi_log_softmax_lastdim(xs[:1]), binding.bi_log_softmax_lastdim(sg[:1]))
+
+
 def test_log_softmax_masked_and_large_entries():
     # -inf entries (a mask) give exactly -inf and weight nothing; large logits
     # do not overflow because the row maximum is subtracted first
