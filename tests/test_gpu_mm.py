@@ -254,6 +254,25 @@ def test_short_a_layout_matches_general_layout_bitwise():
         assert bits_equal(binding.bi_addmm(bias, d, w, out_dtype=torch.float32)[:1], general[:1])
 
 
+@pytest.mark.parametrize("b_layout", ["k", "mn"])
+def test_weight_streaming_launches_match_the_others_bitwise(b_layout):
+    # up to two 256-row tiles (M <= 512) the launch loads the weight with the
+    # evict-first and A with the evict-last L2 priority; larger M, without;
+    # the rows they share must carry the same bits (plain and packed weight)
+    K, N = 1024, 1000
+    a = inputs.normal_bf16((1100, K), 1.0, 93).cuda()
+    w = inputs.normal_bf16((K, N), 0.02, 94)
+    wg = w.t().contiguous().cuda().t() if b_layout == "k" else w.cuda()
+    bias = inputs.normal_bf16((N,), 0.01, 95).cuda()
+    full = binding.bi_addmm(bias, a, wg)                                  # 5 row tiles
+    packed = binding.bi_pack_weight(wg)
+    for M in (1, 33, 256, 257, 511, 512, 513, 768):
+        assert bits_equal(binding.bi_addmm(bias, a[:M], wg), full[:M]), M
+        assert bits_equal(binding.bi_addmm_packed(bias, a[:M], packed), full[:M]), M
+    ref, absum = oracle.mm(a[:3].cpu(), w, bias=bias.cpu())
+    check_tolerance(full[:3], ref, absum, "streamed-weight rows")
+
+
 # -- tile count vs resident CTA pairs ---------------------------------------
 
 @pytest.mark.parametrize("K", [64, 320, 4096])
