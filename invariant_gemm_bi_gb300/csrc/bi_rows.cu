@@ -85,7 +85,16 @@ bi_status launch_row_reduction(int op, const RowParams& rp_in, cudaStream_t stre
     return BI_ERR_INVALID_ARG;
   }
   if (op == kRowRmsNorm) {
-    launch_rmsnorm_rows(T, rp, grid, stream);
+    // More than four blocks per SM: the register-capped form (four resident
+    // blocks per SM instead of two or three; the same bits).
+    bool dense = false;
+    if (T < 1024) {
+      DeviceInfo dev;
+      const bi_status st = current_device_info(&dev, why);
+      if (st != BI_OK) return st;
+      dense = (int64_t)grid.x > 4 * (int64_t)dev.num_sms;
+    }
+    launch_rmsnorm_rows(T, rp, grid, dense, stream);
   } else if (op == kRowLogSoftmax) {
     // 1024-thread teams hold a chunk in registers, one CTA per SM (and a
     // cluster's CTAs within one GPC): when the rows' clusters need more than

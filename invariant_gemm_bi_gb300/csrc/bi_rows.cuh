@@ -388,7 +388,9 @@ int row_cluster_size(int64_t N, int x_kind);
 
 // Launchers of the three operations for team size T (bi_rows_rms.cu,
 // bi_rows_lsm.cu, bi_rows.cu); grid: one block per Team<T>::kRows rows.
-void launch_rmsnorm_rows(int T, const RowParams& rp, dim3 grid, cudaStream_t stream);
+// dense: the RMSNorm kernels' register-capped form (teams under 1024 threads,
+// the common type combinations; the same bits).
+void launch_rmsnorm_rows(int T, const RowParams& rp, dim3 grid, bool dense, cudaStream_t stream);
 // CTAs of the register-resident 1024-thread log-softmax kernel (for rp's
 // types and cluster size) that run at once on the current device; 0 if the
 // occupancy query fails.

@@ -12,8 +12,13 @@ namespace bi {
 template <int T, int W>
 constexpr bool rms_stages_weight() { return W != kNoWeight && T < 1024; }
 
-template <int T, int X, int Y, int W>
-__global__ void __launch_bounds__(Team<T>::kBlock, Team<T>::kBlock >= 512 ? 1 : 512 / Team<T>::kBlock)
+// DENSE (teams under 1024 threads, many blocks): registers capped for four
+// 256-thread blocks per SM instead of two or three -- more rows in flight and
+// a shorter tail when the grid is several waves deep, a slightly longer chain
+// per row when it is not.  The arithmetic is the same.
+template <int T, int X, int Y, int W, bool DENSE = false>
+__global__ void __launch_bounds__(Team<T>::kBlock,
+                                  Team<T>::kBlock >= 512 ? 1 : (DENSE ? 1024 : 512) / Team<T>::kBlock)
     rmsnorm_kernel(const RowParams p) {
   constexpr bool kStage = rms_stages_weight<T, W>();
   constexpr int kBlock = Team<T>::kBlock;
@@ -103,45 +108,55 @@ __global__ void __launch_bounds__(Team<T>::kBlock, Team<T>::kBlock >= 512 ? 1 : 
   if (T == 1024 && rs.cl > 1) cluster_sync_all();  // no CTA leaves while a peer may read its total
 }
 
-template <int T, int X, int Y, int W>
+template <int T, int X, int Y, int W, bool DENSE = false>
 static void launch_rms(const RowParams& rp, dim3 grid, cudaStream_t stream) {
   const size_t smem = rms_stages_weight<T, W>() ? (size_t)rp.N * sizeof(float) : 0;
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(reinterpret_cast<const void*>(&rmsnorm_kernel<T, X, Y, W>),
+    cudaFuncSetAttribute(reinterpret_cast<const void*>(&rmsnorm_kernel<T, X, Y, W, DENSE>),
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  launch_row_kernel(rmsnorm_kernel<T, X, Y, W>, rp, grid, dim3(Team<T>::kBlock), smem, stream);
+  launch_row_kernel(rmsnorm_kernel<T, X, Y, W, DENSE>, rp, grid, dim3(Team<T>::kBlock), smem, stream);
 }
 
+// The dense form exists for the common type combinations: output (and weight,
+// if any) of the input's type.
 template <int T, int X>
-static void launch_rms_x(const RowParams& rp, dim3 grid, cudaStream_t stream) {
+static void launch_rms_x(const RowParams& rp, dim3 grid, bool dense, cudaStream_t stream) {
+  constexpr bool kDenseOk = T < 1024;
   if (!rp.w) {
-    if (rp.y_kind == X)
-      launch_rms<T, X, X, kNoWeight>(rp, grid, stream);
-    else
+    if (rp.y_kind == X) {
+      if (kDenseOk && dense)
+        launch_rms<T, X, X, kNoWeight, kDenseOk>(rp, grid, stream);
+      else
+        launch_rms<T, X, X, kNoWeight>(rp, grid, stream);
+    } else {
       launch_rms<T, X, kKindRuntime, kNoWeight>(rp, grid, stream);
+    }
   } else if (rp.y_kind == X && rp.w_kind == X) {
-    launch_rms<T, X, X, X>(rp, grid, stream);
+    if (kDenseOk && dense)
+      launch_rms<T, X, X, X, kDenseOk>(rp, grid, stream);
+    else
+      launch_rms<T, X, X, X>(rp, grid, stream);
   } else {
     launch_rms<T, X, kKindRuntime, kKindRuntime>(rp, grid, stream);
   }
 }
 
 template <int T>
-static void launch_rms_t(const RowParams& rp, dim3 grid, cudaStream_t stream) {
+static void launch_rms_t(const RowParams& rp, dim3 grid, bool dense, cudaStream_t stream) {
   if (rp.x_kind == 2)
-    launch_rms_x<T, 2>(rp, grid, stream);
+    launch_rms_x<T, 2>(rp, grid, dense, stream);
   else if (rp.x_kind == 1)
-    launch_rms_x<T, 1>(rp, grid, stream);
+    launch_rms_x<T, 1>(rp, grid, dense, stream);
   else
-    launch_rms_x<T, 0>(rp, grid, stream);
+    launch_rms_x<T, 0>(rp, grid, dense, stream);
 }
 
-void launch_rmsnorm_rows(int T, const RowParams& rp, dim3 grid, cudaStream_t stream) {
+void launch_rmsnorm_rows(int T, const RowParams& rp, dim3 grid, bool dense, cudaStream_t stream) {
   switch (T) {
-    case 32: launch_rms_t<32>(rp, grid, stream); break;
-    case 64: launch_rms_t<64>(rp, grid, stream); break;
-    case 256: launch_rms_t<256>(rp, grid, stream); break;
-    default: launch_rms_t<1024>(rp, grid, stream); break;
+    case 32: launch_rms_t<32>(rp, grid, dense, stream); break;
+    case 64: launch_rms_t<64>(rp, grid, dense, stream); break;
+    case 256: launch_rms_t<256>(rp, grid, dense, stream); break;
+    default: launch_rms_t<1024>(rp, grid, false, stream); break;
   }
 }
 

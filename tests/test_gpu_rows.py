@@ -185,6 +185,29 @@ def test_misaligned_and_strided_rows_give_the_same_bits(N):
     assert bool((mbig[1::2] == 7.0).all())
 
 
+# RMSNorm with more than four blocks per SM runs a register-capped form of
+# the same kernel (four resident blocks per SM): the row count picks it, the
+# bits must not depend on it.  Teams of 32 (8 rows a block), 64 (4) and 256
+# (1) threads; weight of the input's type, and no weight.
+DENSE_ROWS = [(torch.bfloat16, 1000, 5200), (torch.bfloat16, 4096, 2600), (torch.float32, 3000, 700),
+              (torch.float16, 12345, 700)]
+
+
+@pytest.mark.parametrize("x_dtype,N,R", DENSE_ROWS)
+def test_rmsnorm_dense_form_equals_small_grids(x_dtype, N, R):
+    x = _x((R, N), x_dtype, 1.0, 12)
+    w = inputs.uniform_bf16((N,), 0.5, 1.5, 13).to(x_dtype)
+    xg, wg = x.cuda(), w.cuda()
+    for wt in (wg, None):
+        full = binding.bi_rmsnorm_lastdim(xg, wt, 1e-6)
+        for r in (0, R // 2, R - 1):
+            assert bits_equal(binding.bi_rmsnorm_lastdim(xg[r:r + 1], wt, 1e-6), full[r:r + 1]), (r, wt is None)
+        assert bits_equal(binding.bi_rmsnorm_lastdim(xg[:9], wt, 1e-6), full[:9])
+        rows = [0, R - 1]
+        ref = oracle.rmsnorm_rows(x[rows], None if wt is None else w, eps=1e-6)
+        check_rmsnorm(full[rows], ref, N, f"rmsnorm dense {x_dtype} {N} w={wt is not None}")
+
+
 # Long rows reduced by clusters of 1024-thread CTAs: when the rows' clusters
 # take more than one wave of SMs the kernel streams each thread's groups from
 # memory on every pass instead of holding them in registers.  The row count
